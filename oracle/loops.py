@@ -1,0 +1,134 @@
+"""ctypes front end of the scalar-loop oracle (``vf_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  Every function takes
+and returns PyTorch CPU tensors of 16-bit elements; bf16 tensors are viewed as
+int16 so that bit patterns (NaN payloads, -0) are what is compared.  Strided
+views are passed as their first element's address plus their element strides,
+exactly as the oracle's loops read them.
+"""
+import ctypes
+
+import torch
+
+from . import build as _build
+
+OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE = 0, 1, 2
+
+_lib = None
+_I64 = ctypes.c_int64
+_P = ctypes.c_void_p
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        l = ctypes.CDLL(_build.build())
+        arr4 = ctypes.POINTER(_I64)
+        for name, args in {
+            "oracle_qkv_pack": [_P, arr4, _I64, _I64, _I64, _I64, _I64, _P],
+            "oracle_qkv_unpack": [_P, _I64, _I64, _I64, _I64, _I64, _P, arr4],
+            "oracle_attn_split": [_P, arr4, _I64, _I64, _I64, _I64, _I64, _P],
+            "oracle_attn_unsplit": [_P, _I64, _I64, _I64, _I64, _I64, _P, arr4],
+            "oracle_head_merge": [_P, _I64, _I64, _I64, _I64, _I64, _P, arr4],
+            "oracle_head_split": [_P, arr4, _I64, _I64, _I64, _I64, _I64, _P],
+            "oracle_piece_table": [ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
+                                   arr4, arr4, arr4, _I64],
+        }.items():
+            f = getattr(l, name)
+            f.argtypes = args
+            f.restype = _I64
+        _lib = l
+    return _lib
+
+
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    if t.device.type != "cpu":
+        raise ValueError("the oracle runs on CPU tensors only")
+    if t.element_size() != 2:
+        raise ValueError("the oracle moves 16-bit elements")
+    return t if t.dtype == torch.int16 else t.view(torch.int16)
+
+
+def _strides(t: torch.Tensor):
+    return (_I64 * t.dim())(*t.stride())
+
+
+def _check(n, expect, what):
+    if n != expect:
+        raise RuntimeError("%s: oracle moved %d elements, expected %d" % (what, n, expect))
+
+
+def qkv_pack(src: torch.Tensor, P: int, C: int) -> torch.Tensor:
+    """QKV destination pack of a [T,3,H,D] view; returns flat packed storage."""
+    s = _bits(src)
+    T, three, H, D = s.shape
+    assert three == 3
+    out = torch.empty(3 * T * H * D, dtype=torch.int16)
+    n = lib().oracle_qkv_pack(s.data_ptr(), _strides(s), T, H, D, P, C, out.data_ptr())
+    _check(n, out.numel(), "qkv_pack")
+    return out
+
+
+def qkv_unpack(packed: torch.Tensor, T: int, H: int, D: int, P: int, C: int) -> torch.Tensor:
+    """Inverse of ``qkv_pack``: flat packed storage back to contiguous [T,3,H,D]."""
+    p = _bits(packed).contiguous()
+    out = torch.empty((T, 3, H, D), dtype=torch.int16)
+    n = lib().oracle_qkv_unpack(p.data_ptr(), T, H, D, P, C, out.data_ptr(), _strides(out))
+    _check(n, p.numel(), "qkv_unpack")
+    return out
+
+
+def attn_split(src: torch.Tensor, P: int, C: int) -> torch.Tensor:
+    """Attention-result split of a [T,H,D] view; returns flat packed storage."""
+    s = _bits(src)
+    T, H, D = s.shape
+    out = torch.empty(T * H * D, dtype=torch.int16)
+    n = lib().oracle_attn_split(s.data_ptr(), _strides(s), T, H, D, P, C, out.data_ptr())
+    _check(n, out.numel(), "attn_split")
+    return out
+
+
+def attn_unsplit(packed: torch.Tensor, T: int, H: int, D: int, P: int, C: int) -> torch.Tensor:
+    """Inverse of ``attn_split``: flat packed storage back to contiguous [T,H,D]."""
+    p = _bits(packed).contiguous()
+    out = torch.empty((T, H, D), dtype=torch.int16)
+    n = lib().oracle_attn_unsplit(p.data_ptr(), T, H, D, P, C, out.data_ptr(), _strides(out))
+    _check(n, p.numel(), "attn_unsplit")
+    return out
+
+
+def head_merge(packed: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
+               out: torch.Tensor = None) -> torch.Tensor:
+    """Returned-head merge of flat packed storage into a [T,H,D] tensor.
+
+    ``out`` may be any non-overlapping strided [T,H,D] int16 view; a
+    contiguous one is allocated when it is omitted.
+    """
+    p = _bits(packed).contiguous()
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.int16)
+    o = _bits(out)
+    assert tuple(o.shape) == (T, H, D)
+    n = lib().oracle_head_merge(p.data_ptr(), T, H, D, P, C, o.data_ptr(), _strides(o))
+    _check(n, T * H * D, "head_merge")
+    return out
+
+
+def head_split(src: torch.Tensor, P: int, C: int) -> torch.Tensor:
+    """Inverse of ``head_merge``: a [T,H,D] view into the merge's packed storage."""
+    s = _bits(src)
+    T, H, D = s.shape
+    out = torch.empty(T * H * D, dtype=torch.int16)
+    n = lib().oracle_head_split(s.data_ptr(), _strides(s), T, H, D, P, C, out.data_ptr())
+    _check(n, out.numel(), "head_split")
+    return out
+
+
+def piece_table(op: int, T: int, H: int, D: int, P: int, C: int):
+    """(tok_start, tok_len, packed_off) lists over (c, p) in storage order."""
+    m = P * C
+    a, b, c = (_I64 * m)(), (_I64 * m)(), (_I64 * m)()
+    n = lib().oracle_piece_table(op, T, H, D, P, C, a, b, c, m)
+    if n != m:
+        raise ValueError("oracle_piece_table rejected its arguments")
+    return list(a), list(b), list(c)

@@ -1,0 +1,270 @@
+/*
+ * Plain CPU oracle for the three exact, direct, destination-major relayouts
+ * around sequence-head (Ulysses) attention: QKV destination pack,
+ * attention-result split and returned-head merge.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker, never the product:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * build, load or call it.  It shares no code, header, table or helper with the
+ * CUDA library; it knows nothing of vectors, tiles, pieces or launches.
+ *
+ * What the method computes.  "Sol-Engine alignment on SM86 and SM89", section
+ * "What is enabled": each direct relayout reads its source through the
+ * source strides and writes destination-major storage exactly once, in place
+ * of a stack/permute/contiguous (pack) or cat/permute/contiguous (merge)
+ * materialisation; every output equals the materialised reference element for
+ * element, and the BF16 values on the wire are unchanged.  The table in that
+ * section names the three operations (QKV destination pack, attention result
+ * split, returned-head merge).  "速度、显存与质量" (speed, memory and
+ * quality), section "剖析单次去噪请求" (profiling one denoising request),
+ * places them on the compute stream: QKV pack -> exchange -> QKV unpack ->
+ * Flash-SDPA -> attention-result pack (the split) -> exchange -> final unpack
+ * (the merge).
+ *
+ * The pages print no index formula.  The readings taken here (all flagged in
+ * the design notes) are:
+ *   - chunk partition of n tokens into C overlap chunks: quota Q(n)=ceil(n/C),
+ *     chunk c covers [min(n,c*Q), min(n,(c+1)*Q)) -- a short tail chunk and
+ *     possibly empty trailing chunks;
+ *   - storage is chunk blocks in order, each block destination-major: [c][p];
+ *   - pack block (c,p) holds head group p (heads p*Hp..p*Hp+Hp-1, Hp=H/P) as
+ *     three consecutive Q, K, V slabs [s][token][head-in-group][d];
+ *   - split partitions the rank-local tokens into P shards of ceil(T/P)
+ *     (short last shard), then each shard n_p into chunks with Q(n_p); block
+ *     (c,p) holds [token][head][d];
+ *   - merge is the inverse of a head-group split: the received block (c,p)
+ *     [token][head-in-group][d] lands in heads p*Hp.. of those tokens.
+ *
+ * Every element is a raw 16-bit pattern: BF16 values, NaN payloads and -0 are
+ * copied verbatim, never converted.
+ *
+ * Each oracle writes the destination with one running cursor k that walks
+ * destination storage in order, so the loop nest *is* the layout and no
+ * destination offset formula exists to get wrong.  Each returns the number
+ * of elements its cursor moved (a negative value on bad arguments).
+ * Strides are in elements.
+ */
+#include <stdint.h>
+
+/* ---- partitions (reading of the four-chunk overlap layout) ------------- */
+
+/* Quota of a chunk (or shard) when n items are cut into `parts` pieces:
+ * ceil(n / parts). */
+static int64_t quota(int64_t n, int64_t parts) {
+    return (n + parts - 1) / parts;
+}
+
+/* First item of part `i` when n items are cut with quota ceil(n/parts). */
+static int64_t part_begin(int64_t n, int64_t parts, int64_t i) {
+    int64_t b = i * quota(n, parts);
+    return b < n ? b : n;
+}
+
+/* One past the last item of part `i`. */
+static int64_t part_end(int64_t n, int64_t parts, int64_t i) {
+    return part_begin(n, parts, i + 1);
+}
+
+static int bad_dims(int64_t T, int64_t H, int64_t D, int64_t P, int64_t C) {
+    return T < 0 || H < 0 || D < 0 || P < 1 || C < 1;
+}
+
+/* ---- QKV destination pack ---------------------------------------------- */
+
+/*
+ * Direct QKV destination pack ("Sol-Engine alignment on SM86 and SM89",
+ * "What is enabled": QKV destination pack).  Source is the fused projection
+ * output viewed as [T][3][H][D] with element strides st[0..3] (token, q/k/v,
+ * head, d).  Destination storage: for each chunk c, for each destination
+ * slot p, for s in (q,k,v), for each token of the chunk, for each head of
+ * group p, for each d.
+ */
+int64_t oracle_qkv_pack(const uint16_t *src, const int64_t st[4],
+                        int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                        uint16_t *dst) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0) return -1;
+    const int64_t Hp = H / P;
+    int64_t k = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        const int64_t t0 = part_begin(T, C, c), t1 = part_end(T, C, c);
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t s = 0; s < 3; ++s)
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int64_t hh = 0; hh < Hp; ++hh) {
+                        const int64_t h = p * Hp + hh;
+                        for (int64_t d = 0; d < D; ++d)
+                            dst[k++] = src[t * st[0] + s * st[1] + h * st[2] + d * st[3]];
+                    }
+    }
+    return k;
+}
+
+/*
+ * Inverse of the pack (the receive side's view when P=1 rank talks to
+ * itself): reads packed storage in the same order and scatters it back into
+ * a [T][3][H][D] tensor with element strides ot[0..3].  Used by the
+ * pack-then-unpack round-trip identity.
+ */
+int64_t oracle_qkv_unpack(const uint16_t *packed,
+                          int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                          uint16_t *out, const int64_t ot[4]) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0) return -1;
+    const int64_t Hp = H / P;
+    int64_t k = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        const int64_t t0 = part_begin(T, C, c), t1 = part_end(T, C, c);
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t s = 0; s < 3; ++s)
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int64_t hh = 0; hh < Hp; ++hh) {
+                        const int64_t h = p * Hp + hh;
+                        for (int64_t d = 0; d < D; ++d)
+                            out[t * ot[0] + s * ot[1] + h * ot[2] + d * ot[3]] = packed[k++];
+                    }
+    }
+    return k;
+}
+
+/* ---- attention-result split -------------------------------------------- */
+
+/*
+ * Direct attention-result split ("Sol-Engine alignment on SM86 and SM89",
+ * "What is enabled": attention result split; the profiling section of
+ * "速度、显存与质量" calls it the attention-result pack).  Source is the
+ * rank-local attention output [T][H][D] (T tokens attended, H heads held)
+ * with element strides st[0..2].  Tokens are cut into P shards with quota
+ * ceil(T/P); shard p (n_p tokens) is cut into C chunks with quota
+ * ceil(n_p/C).  Destination storage: for each chunk c, for each destination
+ * p, the tokens of chunk c of shard p, each as [H][D].
+ */
+int64_t oracle_attn_split(const uint16_t *src, const int64_t st[3],
+                          int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                          uint16_t *dst) {
+    if (bad_dims(T, H, D, P, C)) return -1;
+    int64_t k = 0;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t p = 0; p < P; ++p) {
+            const int64_t a = part_begin(T, P, p);            /* shard start */
+            const int64_t n = part_end(T, P, p) - a;          /* shard length */
+            const int64_t u0 = part_begin(n, C, c), u1 = part_end(n, C, c);
+            for (int64_t u = u0; u < u1; ++u) {
+                const int64_t t = a + u;
+                for (int64_t h = 0; h < H; ++h)
+                    for (int64_t d = 0; d < D; ++d)
+                        dst[k++] = src[t * st[0] + h * st[1] + d * st[2]];
+            }
+        }
+    return k;
+}
+
+/* Inverse of the split: packed storage back to [T][H][D] with strides ot. */
+int64_t oracle_attn_unsplit(const uint16_t *packed,
+                            int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                            uint16_t *out, const int64_t ot[3]) {
+    if (bad_dims(T, H, D, P, C)) return -1;
+    int64_t k = 0;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t p = 0; p < P; ++p) {
+            const int64_t a = part_begin(T, P, p);
+            const int64_t n = part_end(T, P, p) - a;
+            const int64_t u0 = part_begin(n, C, c), u1 = part_end(n, C, c);
+            for (int64_t u = u0; u < u1; ++u) {
+                const int64_t t = a + u;
+                for (int64_t h = 0; h < H; ++h)
+                    for (int64_t d = 0; d < D; ++d)
+                        out[t * ot[0] + h * ot[1] + d * ot[2]] = packed[k++];
+            }
+        }
+    return k;
+}
+
+/* ---- returned-head merge ----------------------------------------------- */
+
+/*
+ * Direct returned-head merge ("Sol-Engine alignment on SM86 and SM89",
+ * "What is enabled": returned-head merge; the profiling section of
+ * "速度、显存与质量" calls it the final unpack).  Source is the received
+ * destination-major storage: for each chunk c (quota ceil(T/C)), for each
+ * source slot p (head group p), the chunk's tokens as [Hp][D].  Destination
+ * is token-major [T][H][D] with element strides dt[0..2]; slot p fills heads
+ * p*Hp .. p*Hp+Hp-1.
+ */
+int64_t oracle_head_merge(const uint16_t *src,
+                          int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                          uint16_t *dst, const int64_t dt[3]) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0) return -1;
+    const int64_t Hp = H / P;
+    int64_t k = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        const int64_t t0 = part_begin(T, C, c), t1 = part_end(T, C, c);
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t t = t0; t < t1; ++t)
+                for (int64_t hh = 0; hh < Hp; ++hh) {
+                    const int64_t h = p * Hp + hh;
+                    for (int64_t d = 0; d < D; ++d)
+                        dst[t * dt[0] + h * dt[1] + d * dt[2]] = src[k++];
+                }
+    }
+    return k;
+}
+
+/* Inverse of the merge (a head-group split): [T][H][D] with strides st into
+ * the merge's source storage. */
+int64_t oracle_head_split(const uint16_t *src, const int64_t st[3],
+                          int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                          uint16_t *packed) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0) return -1;
+    const int64_t Hp = H / P;
+    int64_t k = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        const int64_t t0 = part_begin(T, C, c), t1 = part_end(T, C, c);
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t t = t0; t < t1; ++t)
+                for (int64_t hh = 0; hh < Hp; ++hh) {
+                    const int64_t h = p * Hp + hh;
+                    for (int64_t d = 0; d < D; ++d)
+                        packed[k++] = src[t * st[0] + h * st[1] + d * st[2]];
+                }
+    }
+    return k;
+}
+
+/* ---- piece table ------------------------------------------------------- */
+
+/*
+ * For each (chunk c, destination p), in storage order, the first token, the
+ * token count and the element offset of the block in packed storage,
+ * obtained by advancing a cursor over the blocks in the same order as the
+ * oracles above.
+ * op: 0 = QKV pack, 1 = attention-result split, 2 = returned-head merge.
+ * Returns the number of entries (C*P), or -1 on bad arguments or cap.
+ */
+int64_t oracle_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                           int64_t *tok_start, int64_t *tok_len, int64_t *packed_off,
+                           int64_t cap) {
+    if (bad_dims(T, H, D, P, C) || cap < P * C) return -1;
+    if (op != 1 && H % P != 0) return -1;
+    int64_t k = 0, e = 0;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t p = 0; p < P; ++p, ++e) {
+            int64_t first, count, per_token;
+            if (op == 1) {
+                const int64_t a = part_begin(T, P, p);
+                const int64_t n = part_end(T, P, p) - a;
+                first = a + part_begin(n, C, c);
+                count = part_end(n, C, c) - part_begin(n, C, c);
+                per_token = H * D;
+            } else if (op == 0 || op == 2) {
+                first = part_begin(T, C, c);
+                count = part_end(T, C, c) - first;
+                per_token = (op == 0 ? 3 : 1) * (H / P) * D;
+            } else {
+                return -1;
+            }
+            tok_start[e] = first;
+            tok_len[e] = count;
+            packed_off[e] = k;
+            k += count * per_token;
+        }
+    return e;
+}

@@ -1,0 +1,20 @@
+"""Shared pytest set-up: the ``gpu`` marker, the repo root on sys.path, and
+session fixtures that build the oracle and the CUDA library on demand."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+@pytest.fixture(scope="session")
+def oracle_built():
+    from oracle import build
+    return build.build()
