@@ -1,0 +1,538 @@
+"""Benchmark of the three sequence-head relayouts on GB300.
+
+One step = QKV destination pack + attention-result split + returned-head
+merge over one batch of synthetic input at the pages' shape (T=55,414,
+H=28, D=128, P=2, C=4, bf16 moved as raw 16-bit patterns; pack source with
+row stride 3*H*D+64, split source head-major).  The metric is effective HBM
+GB/s: algorithmic bytes read + written (2 x elements moved x 2 B) over time.
+
+Default arm: the CUDA library.  W untimed warm-up steps, then exactly K steps
+bracketed by a barrier and a device synchronise, timed with CUDA events on
+the launching stream (max over ranks), inputs larger than L2 and two
+rotating buffer sets.  The JSON line also carries the per-op breakdown, the
+roofline of the dominant kernel, the SM clocks sampled during the timed
+region, an end-to-end figure through the public API with pinned host buffers
+(host-to-device copies of the inputs and device-to-host copies of the
+outputs inside the timed region), and the CPU oracle timed on host cores.
+
+``--impl reference``: the CPU oracle as it stands, on the host cores, timed
+on a bounded token sample of the same workload each step.
+
+Several GPUs (torchrun): every rank runs an independent replica of the
+workload on its own GPU (the relayouts have no exchange step on one rank);
+``value`` is the bytes of all ranks over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s (read+write) and % of GB300 peak per relayout op"
+UNIT = "GB/s"
+WORKLOAD = "pages"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["sequence_head_relayout_gb300/csrc/relayout_kernel.cuh",
+                  "sequence_head_relayout_gb300/csrc/vf_relayout.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def op_elements(cfg):
+    T, H, D = cfg.T, cfg.H, cfg.D
+    return {"qkv_pack": 3 * T * H * D, "attn_split": T * H * D, "head_merge": T * H * D}
+
+
+def alg_bytes(elems: int) -> int:
+    return 2 * 2 * elems            # read once + written once, 2 bytes each
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (reported baseline and reference arm); runs in spawned workers
+# ----------------------------------------------------------------------------
+
+def _oracle_worker(job):
+    """One worker: run the C oracle over a token sample of the workload
+    `reps` times; return (seconds, bytes)."""
+    import ctypes
+
+    import numpy as np
+
+    from oracle import build
+    T, H, D, P, C, pad, reps, seed = job
+    lib = ctypes.CDLL(build.LIB)
+    I64 = ctypes.c_int64
+    rng = np.random.default_rng(seed)
+    row = 3 * H * D + pad
+    pack_src = rng.integers(0, 1 << 16, size=T * row, dtype=np.uint16)
+    split_src = rng.integers(0, 1 << 16, size=T * H * D, dtype=np.uint16)   # [H][T][D]
+    merge_src = rng.integers(0, 1 << 16, size=T * H * D, dtype=np.uint16)
+    pack_dst = np.empty(3 * T * H * D, dtype=np.uint16)
+    split_dst = np.empty(T * H * D, dtype=np.uint16)
+    merge_dst = np.empty(T * H * D, dtype=np.uint16)
+    ps = (I64 * 4)(row, H * D, D, 1)
+    ss = (I64 * 3)(D, T * D, 1)
+    ms = (I64 * 3)(H * D, D, 1)
+    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)
+    for f in (lib.oracle_qkv_pack, lib.oracle_attn_split, lib.oracle_head_merge):
+        f.restype = I64
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        lib.oracle_qkv_pack(ptr(pack_src), ps, I64(T), I64(H), I64(D), I64(P), I64(C), ptr(pack_dst))
+        lib.oracle_attn_split(ptr(split_src), ss, I64(T), I64(H), I64(D), I64(P), I64(C),
+                              ptr(split_dst))
+        lib.oracle_head_merge(ptr(merge_src), I64(T), I64(H), I64(D), I64(P), I64(C),
+                              ptr(merge_dst), ms)
+    dt = time.perf_counter() - t0
+    return dt, reps * alg_bytes(5 * T * H * D)
+
+
+class OraclePool:
+    """A spawn-started process pool (safe to create before or after CUDA)."""
+
+    def __init__(self, cores: int):
+        from oracle import build
+        build.build()
+        self.cores = cores
+        self.pool = mp.get_context("spawn").Pool(cores)
+
+    def run(self, cfg, tokens: int, reps: int, seed: int = 0):
+        jobs = [(tokens, cfg.H, cfg.D, cfg.P, cfg.C, cfg.pad, reps, seed + i)
+                for i in range(self.cores)]
+        t0 = time.perf_counter()
+        res = self.pool.map(_oracle_worker, jobs)
+        wall = time.perf_counter() - t0
+        return wall, sum(b for _, b in res), max(t for t, _ in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def calibrate_tokens(pool: OraclePool, cfg, seconds_per_step: float) -> int:
+    """Token count whose oracle pass takes about `seconds_per_step` per worker."""
+    probe = 256
+    _, _, t = pool.run(cfg, probe, 1)
+    per_token = max(t / probe, 1e-9)
+    return int(max(16, min(cfg.T, seconds_per_step / per_token)))
+
+
+def cpu_baseline(cfg, budget_s: float = 10.0, cores: int = None):
+    cores = cores or os.cpu_count() or 1
+    pool = OraclePool(cores)
+    try:
+        tokens = calibrate_tokens(pool, cfg, budget_s / 3)
+        wall, nbytes, _ = pool.run(cfg, tokens, 3, seed=100)
+    finally:
+        pool.close()
+    return {"value": round(nbytes / wall / 1e9, 3), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": "%d of %d tokens (H=%d, D=%d, P=%d, C=%d, padded-row pack source, "
+                      "head-major split source), one independent sample per core, 3 passes "
+                      "of pack+split+merge, %.1f s wall" % (tokens, cfg.T, cfg.H, cfg.D, cfg.P,
+                                                             cfg.C, wall)}
+
+
+# ----------------------------------------------------------------------------
+# Clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(self.REASONS, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in d and d[key]:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """ncu DRAM bytes per launch for the current kernel source, else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return d
+
+
+def make_set(cfg, dev, seed_shift, ops=("qkv_pack", "attn_split", "head_merge")):
+    import torch
+
+    from sequence_head_relayout_gb300 import workloads as W
+    n = op_elements(cfg)
+    s = {}
+    if "qkv_pack" in ops:
+        s["pack_src"], s["pack_base"] = W.pack_source(cfg, device=dev, seed=cfg.seed + seed_shift)
+        s["pack_dst"] = torch.empty(n["qkv_pack"], dtype=torch.int16, device=dev)
+    if "attn_split" in ops:
+        s["split_src"], s["split_base"] = W.split_source(cfg, device=dev,
+                                                         seed=cfg.seed + seed_shift)
+        s["split_dst"] = torch.empty(n["attn_split"], dtype=torch.int16, device=dev)
+    if "head_merge" in ops:
+        s["merge_src"] = W.merge_source(cfg, device=dev, seed=cfg.seed + seed_shift)
+        s["merge_dst"] = torch.empty((cfg.T, cfg.H, cfg.D), dtype=torch.int16, device=dev)
+    return s
+
+
+def run_step(vf, cfg, s, events=None):
+    """Enqueue the step's relayouts; events[i] is recorded before op i and
+    events[-1] after the last one."""
+    k = 0
+    if events:
+        events[0].record()
+    if "pack_src" in s:
+        vf.qkv_pack(s["pack_src"], cfg.P, cfg.C, out=s["pack_dst"])
+        k += 1
+        if events:
+            events[k].record()
+    if "split_src" in s:
+        vf.attn_split(s["split_src"], cfg.P, cfg.C, out=s["split_dst"])
+        k += 1
+        if events:
+            events[k].record()
+    if "merge_src" in s:
+        vf.head_merge(s["merge_src"], cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, out=s["merge_dst"])
+        k += 1
+        if events:
+            events[k].record()
+
+
+def launches_per_step(cfg, nops: int) -> int:
+    per_launch = 64           # pieces per launch in the library
+    return nops * -(-cfg.P * cfg.C // per_launch)
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import sequence_head_relayout_gb300 as vf
+    from sequence_head_relayout_gb300 import workloads as W
+
+    cfg = W.CONFIGS[args.config]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    vf.lib()
+
+    order = ("qkv_pack", "attn_split", "head_merge")
+    ops_run = tuple(o for o in order if not args.only or o in args.only)
+    sets = [make_set(cfg, dev, 17 * i, ops_run) for i in range(args.sets)]
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        run_step(vf, cfg, sets[i % len(sets)])
+    barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops_run) + 1)]
+          for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    start.record()
+    for i in range(K):
+        run_step(vf, cfg, sets[i % len(sets)], ev[i])
+    end.record()
+    barrier()
+    clock_info = clocks.stop()
+
+    total_ms = start.elapsed_time(end)
+    per_op_ms = {name: [] for name in ops_run}
+    for e in ev:
+        for j, name in enumerate(ops_run):
+            per_op_ms[name].append(e[j].elapsed_time(e[j + 1]))
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+
+    elems = op_elements(cfg)
+    step_bytes = sum(alg_bytes(elems[n]) for n in ops_run)
+    value = world * K * step_bytes / (max_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    ops = {}
+    for name, ts in per_op_ms.items():
+        med = statistics.median(ts)
+        mean = statistics.fmean(ts)
+        b = alg_bytes(elems[name])
+        ops[name] = {"bytes": b, "median_us": round(med * 1e3, 2),
+                     "mean_us": round(mean * 1e3, 2),
+                     "min_us": round(min(ts) * 1e3, 2),
+                     "p90_us": round(sorted(ts)[int(0.9 * (len(ts) - 1))] * 1e3, 2),
+                     "gbs": round(b / (med / 1e3) / 1e9, 1),
+                     "frac_of_peak": round(b / (med / 1e3) / 1e9 / peak, 4)}
+    if "attn_split" in ops:
+        ops["attn_split"]["per_chunk_us"] = round(ops["attn_split"]["median_us"] / cfg.C, 2)
+
+    dominant = max(per_op_ms, key=lambda k: sum(per_op_ms[k]))
+    avg_s = statistics.fmean(per_op_ms[dominant]) / 1e3
+    achieved = alg_bytes(elems[dominant]) / avg_s / 1e9
+    traffic = recorded_traffic()
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": (traffic or {}).get(dominant),
+                "algorithmic_bytes": alg_bytes(elems[dominant])}
+
+    e2e = None
+    if not args.no_e2e and not args.only:
+        del sets
+        torch.cuda.empty_cache()
+        e2e = e2e_arm(args, cfg, dev, world)
+
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(max_ms / K, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 bit patterns)",
+            "config": {"workload": "%s: T=%d H=%d D=%d P=%d C=%d" % (cfg.name, cfg.T, cfg.H,
+                                                                    cfg.D, cfg.P, cfg.C),
+                       "pack_source": "row stride %d elements (3*H*D+%d)" % (
+                           3 * cfg.H * cfg.D + cfg.pad, cfg.pad),
+                       "split_source": "head-major [H,T,D] viewed as [T,H,D]",
+                       "merge_destination": "contiguous [T,H,D]",
+                       "step": " + ".join(ops_run),
+                       "l2": "inputs larger than L2 (each op reads >= 397 MB), "
+                             "%d rotating buffer set(s)" % args.sets,
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "ops": ops,
+            "roofline": roofline,
+            "clocks": clock_info,
+            "gpu_launches": K * launches_per_step(cfg, len(ops_run)),
+            "e2e": e2e,
+        }
+    return line
+
+
+def e2e_arm(args, cfg, dev, world):
+    """Same metric through the public API from pinned host buffers: every
+    step copies its inputs host->device, runs the three relayouts and copies
+    the outputs device->host."""
+    import torch
+
+    import sequence_head_relayout_gb300 as vf
+    from sequence_head_relayout_gb300 import workloads as W
+
+    d = make_set(cfg, dev, 33)
+    host = {k: torch.empty(d[k].shape, dtype=torch.int16, pin_memory=True)
+            for k in ("pack_base", "split_base", "merge_src", "pack_dst", "split_dst",
+                      "merge_dst")}
+    host["pack_base"].copy_(d["pack_base"])
+    host["split_base"].copy_(d["split_base"])
+    host["merge_src"].copy_(d["merge_src"])
+    torch.cuda.synchronize()
+    h2d = sum(host[k].numel() * 2 for k in ("pack_base", "split_base", "merge_src"))
+    d2h = sum(host[k].numel() * 2 for k in ("pack_dst", "split_dst", "merge_dst"))
+
+    def step():
+        d["pack_base"].copy_(host["pack_base"], non_blocking=True)
+        d["split_base"].copy_(host["split_base"], non_blocking=True)
+        d["merge_src"].copy_(host["merge_src"], non_blocking=True)
+        run_step(vf, cfg, d)
+        host["pack_dst"].copy_(d["pack_dst"], non_blocking=True)
+        host["split_dst"].copy_(d["split_dst"], non_blocking=True)
+        host["merge_dst"].copy_(d["merge_dst"], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    step_bytes = sum(alg_bytes(x) for x in op_elements(cfg).values())
+    return {"value": round(world * n * step_bytes / (ms / 1e3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": round(ms / n, 3)}
+
+
+# ----------------------------------------------------------------------------
+# Reference arm: the oracle on host cores
+# ----------------------------------------------------------------------------
+
+def reference_arm(args, world):
+    from sequence_head_relayout_gb300 import workloads as W
+    cfg = W.CONFIGS[args.config]
+    cores = args.cpu_cores or os.cpu_count() or 1
+    pool = OraclePool(cores)
+    try:
+        budget = max(0.02, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+        tokens = calibrate_tokens(pool, cfg, budget)
+        for _ in range(args.warmup):
+            pool.run(cfg, tokens, 1)
+        total_wall, total_bytes = 0.0, 0
+        for i in range(args.steps):
+            wall, nbytes, _ = pool.run(cfg, tokens, 1, seed=i)
+            total_wall += wall
+            total_bytes += nbytes
+    finally:
+        pool.close()
+    value = total_bytes / total_wall / 1e9
+    sample = ("%d of %d tokens per core per step (H=%d, D=%d, P=%d, C=%d), pack+split+merge"
+              % (tokens, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_wall / max(1, args.steps) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded uniform 16-bit patterns)",
+        "config": {"workload": "%s: T=%d H=%d D=%d P=%d C=%d" % (cfg.name, cfg.T, cfg.H, cfg.D,
+                                                                cfg.P, cfg.C),
+                   "step": "qkv_pack + attn_split + head_merge (CPU oracle)",
+                   "parallelism": "%d host processes" % cores},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-cores", type=int, default=0)
+    ap.add_argument("--only", nargs="+", choices=["qkv_pack", "attn_split", "head_merge"],
+                    help="time only these relayouts (profiling runs)")
+    ap.add_argument("--sets", type=int, default=2, help="rotating input/output buffer sets")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = gpu_arm(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            from sequence_head_relayout_gb300 import workloads as W
+            line["cpu_baseline"] = cpu_baseline(W.CONFIGS[args.config],
+                                                cores=args.cpu_cores or None)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * vf_relayout.h -- C ABI of libvf_relayout.so: exact, direct,
+ * destination-major relayouts around sequence-head (Ulysses-style)
+ * attention, as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Source of the operations: "Sol-Engine alignment on SM86 and SM89", section
+ * "What is enabled" (with its Chinese twin "SM86 与 SM89 上的 Sol-Engine
+ * 对齐", section "当前启用的优化").  The two-device sequence-head path packs
+ * QKV and merges the returned attention heads with direct relayouts: each
+ * reads its source through the source strides and writes destination-major
+ * storage once, in place of stack/permute/contiguous or
+ * cat/permute/contiguous materialisations, keeping the BF16 values and the
+ * exchange's wire format.  The same table lists the attention-result split.
+ * "速度、显存与质量" (speed, memory and quality), section "剖析单次去噪请求",
+ * orders them on the compute stream: QKV pack -> exchange -> QKV unpack ->
+ * Flash-SDPA -> attention-result pack (the split) -> exchange -> final unpack
+ * (the merge).
+ *
+ * The pages give no index formula; this library fixes one reading:
+ *   Hp = H / P heads per destination slot (H % P == 0 for pack and merge).
+ *   Chunk partition of n tokens into C overlap chunks: quota Q(n) =
+ *   ceil(n / C); chunk c covers tokens [min(n, c*Q), min(n, (c+1)*Q)), so the
+ *   last non-empty chunk may be short and trailing chunks may be empty.
+ *   Packed storage is chunk blocks in order, each destination-major: block
+ *   (c, p) for c = 0..C-1 (outer), p = 0..P-1 (inner), no gaps, no padding.
+ *
+ * Elements are 16-bit (BF16) and are moved as raw bit patterns: NaN payloads,
+ * -0 and denormals arrive unchanged.  Strides are in ELEMENTS, int64, and
+ * must be non-negative.  All offsets are computed in 64-bit arithmetic.
+ *
+ * Ownership and concurrency: the caller owns every buffer.  The library
+ * allocates no memory, keeps no global state, never synchronises, and is
+ * safe to call from several host threads.  Work is enqueued on `stream`
+ * (NULL = the legacy default stream) of the current device; every pointer
+ * must be accessible from that device (device, managed or mapped pinned
+ * memory).  The call returns once the kernels are enqueued.
+ *
+ * Errors: every function returns VF_OK (0) or a negative vf_status.  All
+ * argument checks run on the host before anything is enqueued, so a
+ * rejected call leaves dst untouched.  A call whose element count is zero
+ * (T, H or D equal to 0) returns VF_OK without touching the GPU.
+ */
+#ifndef VF_RELAYOUT_H
+#define VF_RELAYOUT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t and CUstream; declared here so that C callers
+ * need no CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *vf_stream_t;
+
+typedef enum vf_status {
+    VF_OK = 0,
+    /* NULL pointer with a non-empty tensor, negative dimension or stride,
+     * P < 1, C < 1, P * C > 2^20, H % P != 0 (pack, merge), T > 2^30,
+     * NULL strides for the pack or the split, a pointer that is not 2-byte
+     * aligned, a merge destination view that overlaps itself, an unknown op,
+     * or a pointer the current device cannot access (pageable host memory
+     * unknown to CUDA, another GPU's memory). */
+    VF_ERR_ARG = -1,
+    /* An element count, offset or byte extent does not fit in int64. */
+    VF_ERR_OVERFLOW = -2,
+    /* The destination's byte range overlaps the bytes the source view
+     * addresses (the relayouts are not in-place). */
+    VF_ERR_ALIAS = -3,
+    /* The CUDA runtime reported an error while querying a pointer or
+     * enqueueing a kernel (cudaGetLastError after the launch). */
+    VF_ERR_CUDA = -4,
+    /* cap is smaller than the number of entries to write. */
+    VF_ERR_CAPACITY = -5
+} vf_status;
+
+typedef enum vf_op {
+    VF_OP_QKV_PACK = 0,
+    VF_OP_ATTN_SPLIT = 1,
+    VF_OP_HEAD_MERGE = 2
+} vf_op;
+
+/*
+ * QKV destination pack.  ("Sol-Engine alignment on SM86 and SM89", "What is
+ * enabled": QKV destination pack; the source is the merged QKV projection's
+ * output, "one wide GEMM before splitting views", table "Upstream gap and
+ * disposition", row "Merged QKV projection".)
+ *
+ * src:         16-bit elements of a logical [T][3][H][D] view (token, q/k/v,
+ *              head, d); src_strides[4] = its element strides in that order.
+ * dst:         3*T*H*D contiguous elements, written once.  Block (c, p) is
+ *              head group p of chunk c's tokens as three consecutive slabs
+ *              s = q, k, v, each [L_c][Hp][D]:
+ *                dst[off(c,p) + ((s*L_c + tc)*Hp + hh)*D + d]
+ *                  = src[t][s][p*Hp + hh][d],  t = first token of c + tc.
+ * Requires H % P == 0.
+ */
+int vf_qkv_pack(const void *src, const int64_t src_strides[4],
+                int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                void *dst, vf_stream_t stream);
+
+/*
+ * Attention-result split.  ("Sol-Engine alignment on SM86 and SM89", "What is
+ * enabled": attention result split; "速度、显存与质量", "剖析单次去噪请求":
+ * the attention-result pack before the outbound exchange.)
+ *
+ * src:         16-bit elements of the rank-local attention output, a logical
+ *              [T][H][D] view (T tokens attended, H heads held);
+ *              src_strides[3] = its element strides (token, head, d), e.g.
+ *              (D, T*D, 1) for a head-major [H][T][D] buffer.
+ * dst:         T*H*D contiguous elements, written once.  Tokens are cut into
+ *              P destination shards with quota ceil(T/P); shard p (n_p
+ *              tokens) into C chunks with quota ceil(n_p/C).  Block (c, p)
+ *              is chunk c of shard p as [L][H][D].
+ * No constraint between H and P.
+ */
+int vf_attn_split(const void *src, const int64_t src_strides[3],
+                  int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                  void *dst, vf_stream_t stream);
+
+/*
+ * Returned-head merge.  ("Sol-Engine alignment on SM86 and SM89", "What is
+ * enabled": returned-head merge, replacing cat/permute/contiguous;
+ * "速度、显存与质量", "剖析单次去噪请求": the final unpack.)
+ *
+ * src:         T*H*D contiguous elements of received destination-major
+ *              storage: block (c, p) is chunk c's tokens for head group p,
+ *              [L_c][Hp][D].  (The packed side is always this canonical
+ *              layout: with a short tail chunk it is not a uniformly
+ *              strided tensor.)
+ * dst:         16-bit elements of a logical [T][H][D] view, written once;
+ *              dst_strides[3] = its element strides (token, head, d), or
+ *              NULL for contiguous (H*D, D, 1).  The view must not overlap
+ *              itself (checked: sorted by stride, each stride must exceed
+ *              the span of the smaller ones).
+ *                dst[t][p*Hp + hh][d] = src[off(c,p) + (tc*Hp + hh)*D + d].
+ * Requires H % P == 0.
+ */
+int vf_head_merge(const void *src, const int64_t dst_strides[3],
+                  int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                  void *dst, vf_stream_t stream);
+
+/*
+ * Number of elements of the packed side of `op` (3*T*H*D for the pack,
+ * T*H*D otherwise), or a negative vf_status on bad arguments or overflow.
+ * Pure host function.
+ */
+int64_t vf_packed_elems(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C);
+
+/*
+ * The piece table of `op`: for each (c, p) in storage order (c outer), the
+ * first token (tok_start; for the split, counted in the source's token
+ * numbering), the token count (tok_len) and the element offset of the block
+ * in packed storage (packed_off).  Writes C*P entries into each caller-owned
+ * array of capacity `cap` and returns C*P, or a negative vf_status
+ * (VF_ERR_CAPACITY when cap < C*P).  Pure host function.
+ */
+int64_t vf_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                       int64_t *tok_start, int64_t *tok_len, int64_t *packed_off,
+                       int64_t cap);
+
+/* Static, NUL-terminated description of a vf_status value. */
+const char *vf_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VF_RELAYOUT_H */

@@ -1,0 +1,118 @@
+// Device side of the three relayouts: one row-block copy kernel.
+//
+// All three operations ("Sol-Engine alignment on SM86 and SM89", section
+// "What is enabled": QKV destination pack, attention result split,
+// returned-head merge) move whole token rows between a contiguous *packed*
+// side (the exchange buffer, destination-major) and a *strided* side (the
+// caller's tensor view).  The host cuts the work into pieces; a piece is one
+// (chunk, destination) block of the packed storage:
+//
+//   packed  : rows x (heads x D) contiguous elements starting at packed_off
+//             (+ slab * rows * heads * D for the pack's q/k/v slabs);
+//   strided : element (row, head, d) at strided_off + slab * slab_stride
+//             + row * row_stride + head * head_stride + d * d_stride.
+//
+// There is no element-level transpose: the (token, head) interchange between
+// the two sides happens at the granularity of whole D-element head rows (at
+// least 32 B, one DRAM sector, for every shape accepted on the vector paths),
+// so both sides stay sector-complete with plain 16-byte loads and stores and
+// no shared-memory staging.  The block is a 3-D thread array
+// (x: VW-element vector within a head row, y: head, z: row) so the address of
+// a thread is a sum of products (the only divisions are block-uniform), and a
+// warp covers consecutive packed vectors.  Each thread keeps kRowsPerThread
+// independent loads in flight before it stores.  Offsets are 64-bit
+// throughout; a source view whose span crosses 2^31 elements is addressed
+// correctly (the FP8 section of "速度、显存与质量" notes the same
+// widen-before-multiplying rule for views past 2^31 elements).
+#pragma once
+
+#include <cstdint>
+
+namespace vf {
+
+constexpr int kMaxPieces = 64;       // pieces per launch (kernel parameter space)
+constexpr int kRowsPerThread = 4;    // independent loads in flight per thread
+constexpr int kMaxThreads = 512;     // threads per block, upper bound
+
+struct Piece {
+    int64_t packed_off;    // element offset of the block in packed storage
+    int64_t strided_off;   // element offset of the block's first row, strided side
+    int64_t rows;          // tokens in the block
+};
+
+struct Args {
+    const uint16_t *src;
+    uint16_t *dst;
+    int64_t row_stride;    // strided side, between consecutive rows (tokens)
+    int64_t head_stride;   // strided side, between heads of one row
+    int64_t d_stride;      // strided side, along d (1 on every vector path)
+    int64_t slab_stride;   // strided side, between the pack's q/k/v slabs
+    int32_t heads;         // heads per packed row
+    int32_t D;             // elements per head row
+    int32_t npieces;
+    int32_t hchunks;       // ceil(heads / blockDim.y)
+    int32_t dchunks;       // ceil(D / VW / blockDim.x)
+    int32_t z_base;        // first folded z index of this launch
+    Piece pieces[kMaxPieces];
+};
+
+template <int VW> struct Vec;
+template <> struct Vec<8> { using T = uint4; };
+template <> struct Vec<4> { using T = uint2; };
+template <> struct Vec<2> { using T = unsigned int; };
+template <> struct Vec<1> { using T = unsigned short; };
+
+// Every element is touched exactly once: read through the read-only path
+// without allocating in L1, and store with the streaming (evict-first) hint.
+template <typename V>
+__device__ __forceinline__ V load_once(const uint16_t *p) {
+    return __ldcs(reinterpret_cast<const V *>(p));
+}
+
+template <typename V>
+__device__ __forceinline__ void store_once(uint16_t *p, const V &v) {
+    __stcs(reinterpret_cast<V *>(p), v);
+}
+
+// Grid: x = groups of kRowsPerThread * blockDim.z rows, y = piece,
+// z = (slab, head chunk, d chunk) folded, offset by z_base.  Block: x = vector
+// within a head row, y = head, z = row.  A thread copies one vector of each of
+// its kRowsPerThread rows: all loads first, then all stores.
+template <int VW, bool kPackedIsDst>
+__global__ void __launch_bounds__(kMaxThreads)
+relayout_rows(const __grid_constant__ Args a) {
+    using V = typename Vec<VW>::T;
+    const Piece &pc = a.pieces[blockIdx.y];
+    const int rows = int(pc.rows);
+    const int rstep = int(blockDim.z);
+    const int row0 = int(blockIdx.x) * (kRowsPerThread * rstep) + int(threadIdx.z);
+    const int per_slab = a.hchunks * a.dchunks;
+    const int z = int(blockIdx.z) + a.z_base;
+    const int slab = z / per_slab;                         // block-uniform
+    const int rem = z - slab * per_slab;
+    const int hc = rem / a.dchunks;
+    const int hh = hc * int(blockDim.y) + int(threadIdx.y);
+    const int dx = (rem - hc * a.dchunks) * int(blockDim.x) + int(threadIdx.x);
+    if (row0 >= rows || hh >= a.heads || dx * VW >= a.D) return;
+
+    const int64_t R = int64_t(a.heads) * a.D;              // packed row length
+    const int64_t po = pc.packed_off + int64_t(slab) * rows * R + int64_t(row0) * R
+                     + int64_t(hh) * a.D + int64_t(dx) * VW;
+    const int64_t so = pc.strided_off + int64_t(slab) * a.slab_stride
+                     + int64_t(row0) * a.row_stride + int64_t(hh) * a.head_stride
+                     + int64_t(dx) * VW * a.d_stride;
+    const uint16_t *s = a.src + (kPackedIsDst ? so : po);
+    uint16_t *d = a.dst + (kPackedIsDst ? po : so);
+    const int64_t s_step = int64_t(rstep) * (kPackedIsDst ? a.row_stride : R);
+    const int64_t d_step = int64_t(rstep) * (kPackedIsDst ? R : a.row_stride);
+
+    V v[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r)
+        if (row0 + r * rstep < rows) v[r] = load_once<V>(s + r * s_step);
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r)
+        if (row0 + r * rstep < rows) store_once<V>(d + r * d_step, v[r]);
+}
+
+}  // namespace vf

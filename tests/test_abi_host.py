@@ -1,0 +1,154 @@
+"""The C ABI on the host, without a GPU.
+
+Checks that ``libvf_relayout.so`` loads and exports every function that
+``include/*.h`` declares, that its pure-host functions (sizes and piece
+tables) agree with the oracle and the hand-derived fixtures, and that every
+rejected argument is rejected before the library touches CUDA (fake pointer
+values are safe here because nothing is dereferenced or launched).
+"""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import sequence_head_relayout_gb300 as vf
+from oracle import loops
+from tests import _golden
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+I64 = ctypes.c_int64
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sequence_head_relayout_gb300 import _build
+    _build.build()
+    return vf.lib()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(vf_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for want in ("vf_qkv_pack", "vf_attn_split", "vf_head_merge", "vf_packed_elems",
+                 "vf_piece_table", "vf_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", vf.LIB_PATH], check=True,
+                         capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (vf_[a-z0-9_]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(L, n)
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "vf_relayout.h"\nint main(void){return VF_OK;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-c", str(src), "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_status_strings(L):
+    for s in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(L.vf_status_string(s), bytes) and L.vf_status_string(s)
+
+
+def test_packed_elems_matches_page_byte_counts(L):
+    g = _golden.load("page_byte_counts.txt")
+    T, H, D, P, C = g["T"], g["H"], g["D"], g["P"], g["C"]
+    assert vf.packed_elems(vf.OP_QKV_PACK, T, H, D, P, C) * 2 == g["pack_direct_bytes"]
+    assert vf.packed_elems(vf.OP_HEAD_MERGE, T, H, D, P, C) * 2 == g["merge_direct_bytes"]
+    assert vf.packed_elems(vf.OP_ATTN_SPLIT, T, H, D, P, C) * 2 == C * g["split_per_call_bytes"]
+
+
+def test_piece_tables_match_hand_derivation(L):
+    g = _golden.load("piece_tables_ragged.txt")
+    for op, key in ((vf.OP_QKV_PACK, "pack"), (vf.OP_ATTN_SPLIT, "split"),
+                    (vf.OP_HEAD_MERGE, "merge")):
+        a, b, c = vf.piece_table(op, 55413, 32, 64, 4, 4)
+        assert a == g[key + "_tok_start"]
+        assert b == g[key + "_tok_len"]
+        assert c == g[key + "_packed_off"]
+
+
+@pytest.mark.parametrize("shape", [(0, 4, 8, 2, 3), (1, 2, 2, 2, 5), (5, 4, 1, 4, 2),
+                                   (55414, 28, 128, 2, 4), (200000, 32, 128, 8, 4),
+                                   (37, 6, 16, 3, 7), (4, 6, 2, 6, 16)])
+def test_piece_tables_match_oracle(L, shape):
+    T, H, D, P, C = shape
+    for op in (0, 1, 2):
+        assert vf.piece_table(op, T, H, D, P, C) == loops.piece_table(op, T, H, D, P, C)
+
+
+def _call(L, fn, src, strides, T, H, D, P, C, dst):
+    arr = None if strides is None else (I64 * len(strides))(*strides)
+    return getattr(L, fn)(src, arr, T, H, D, P, C, dst, None)
+
+
+FAKE_SRC, FAKE_DST = 1 << 40, 1 << 41
+
+
+@pytest.mark.parametrize("args,status", [
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 3, 1, FAKE_DST), -1),   # H % P
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 0, 1, FAKE_DST), -1),   # P < 1
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 2, 0, FAKE_DST), -1),   # C < 1
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), -1, 4, 8, 2, 1, FAKE_DST), -1),  # T < 0
+    (("vf_qkv_pack", FAKE_SRC, (96, -32, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -1),  # negative stride
+    (("vf_qkv_pack", FAKE_SRC, None, 4, 4, 8, 2, 1, FAKE_DST), -1),             # no strides
+    (("vf_qkv_pack", None, (96, 32, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -1),       # null src
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 2, 1, None), -1),       # null dst
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), (1 << 30) + 1, 4, 8, 2, 1, FAKE_DST), -1),  # T > 2^30
+    (("vf_qkv_pack", FAKE_SRC + 1, (96, 32, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -1),   # odd address
+    (("vf_head_merge", FAKE_SRC, None, 4, 4, 8, 2, 1, FAKE_DST + 3), -1),           # odd address
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 2, 1 << 21, FAKE_DST), -1),  # P*C > 2^20
+    (("vf_qkv_pack", FAKE_SRC, (1 << 62, 32, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -2),  # offset overflow
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 1 << 30, 1 << 20, 1 << 12, 2, 1, FAKE_DST), -2),
+    (("vf_attn_split", FAKE_SRC, (1 << 40, 8, 1), 1 << 30, 4, 8, 2, 1, FAKE_DST), -2),
+    (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 2, 1, FAKE_SRC + 64), -3),  # alias
+    (("vf_attn_split", FAKE_SRC, (32, 8, 1), 4, 4, 8, 3, 1, FAKE_SRC + 10), -3),
+    (("vf_attn_split", FAKE_SRC, None, 4, 4, 8, 3, 1, FAKE_DST), -1),
+    (("vf_head_merge", FAKE_SRC, (32, 8, 1), 4, 4, 8, 3, 1, FAKE_DST), -1),     # H % P
+    (("vf_head_merge", FAKE_SRC, (0, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -1),      # overlapping dst
+    (("vf_head_merge", FAKE_SRC, (8, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -1),      # overlapping dst
+    (("vf_head_merge", FAKE_SRC, None, 4, 4, 8, 2, 1, FAKE_SRC + 2), -3),       # alias
+])
+def test_rejected_before_cuda(L, args, status):
+    assert _call(L, *args) == status
+
+
+@pytest.mark.parametrize("fn,strides", [("vf_qkv_pack", (0, 0, 0, 0)), ("vf_attn_split", (0, 0, 0)),
+                                        ("vf_head_merge", None)])
+def test_empty_calls_return_ok_without_cuda(L, fn, strides):
+    # T = 0, H = 0 or D = 0: nothing to move, no pointer is needed
+    for T, H, D in ((0, 4, 8), (4, 0, 8), (4, 4, 0)):
+        assert _call(L, fn, None, strides, T, H, D, 2, 3, None) == 0
+
+
+def test_piece_table_capacity(L):
+    a = (I64 * 3)()
+    assert L.vf_piece_table(0, 10, 4, 8, 2, 2, a, a, a, 3) == -5
+    assert L.vf_piece_table(9, 10, 4, 8, 2, 2, a, a, a, 3) == -1
+    assert L.vf_packed_elems(0, 10, 3, 8, 2, 2) == -1
+    assert L.vf_packed_elems(1, 10, 3, 8, 2, 2) == 240
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+    with pytest.raises(ValueError):
+        vf.qkv_pack(torch.zeros((4, 3, 2, 8), dtype=torch.int16), 2, 1)
+    with pytest.raises(ValueError):
+        vf.attn_split(torch.zeros((4, 2, 8), dtype=torch.bfloat16), 2, 1)

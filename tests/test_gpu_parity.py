@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA relayouts against the CPU oracle, bit for bit.
+
+Every test feeds the same seeded tensors to the library (through its C ABI
+via the ctypes binding) and to the scalar-loop oracle, and compares the 16-bit
+patterns exactly (NaN payloads and -0 included).  The full-size workloads are
+checked in full, with the same entry points and therefore the same launch
+configuration as the benchmark.
+"""
+import pytest
+import torch
+
+import sequence_head_relayout_gb300 as vf
+from oracle import loops
+from sequence_head_relayout_gb300 import workloads as W
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("oracle_built")]
+
+DEV = torch.device("cuda:0")
+CONFIG_NAMES = ["tiny", "4k", "pages", "ragged", "large"]
+
+
+def same_bits(gpu_out: torch.Tensor, want: torch.Tensor) -> bool:
+    """Exact comparison of 16-bit patterns; the oracle side is moved to the GPU."""
+    a = gpu_out.view(torch.int16)
+    b = want.view(torch.int16).to(a.device)
+    return a.shape == b.shape and torch.equal(a, b)
+
+
+def first_mismatch(gpu_out, want):
+    a = gpu_out.reshape(-1).view(torch.int16)
+    b = want.reshape(-1).view(torch.int16).to(a.device)
+    bad = (a != b).nonzero()
+    return None if bad.numel() == 0 else int(bad[0])
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    vf.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+# --------------------------------------------------------------------------
+# Full configurations
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", CONFIG_NAMES)
+def test_qkv_pack_config(name):
+    cfg = W.CONFIGS[name]
+    src_gpu, base = W.pack_source(cfg, device=DEV)
+    got = vf.qkv_pack(src_gpu, cfg.P, cfg.C)
+    src_cpu = src_gpu.cpu()
+    del base, src_gpu
+    want = loops.qkv_pack(src_cpu, cfg.P, cfg.C)
+    assert got.numel() == want.numel()
+    assert same_bits(got, want), first_mismatch(got, want)
+    if cfg.pack_src == "padded_rows":
+        # the padding sentinel is never read
+        assert not bool((got == W._as_i16(W.PAD_SENTINEL)).any())
+
+
+@pytest.mark.parametrize("name", CONFIG_NAMES)
+def test_attn_split_config(name):
+    cfg = W.CONFIGS[name]
+    src_gpu, _ = W.split_source(cfg, device=DEV)
+    got = vf.attn_split(src_gpu, cfg.P, cfg.C)
+    want = loops.attn_split(src_gpu.cpu(), cfg.P, cfg.C)
+    assert same_bits(got, want), first_mismatch(got, want)
+
+
+@pytest.mark.parametrize("name", CONFIG_NAMES)
+def test_head_merge_config(name):
+    cfg = W.CONFIGS[name]
+    src_gpu = W.merge_source(cfg, device=DEV)
+    out, base = W.merge_destination(cfg, device=DEV, fill=0x7FA5)
+    vf.head_merge(src_gpu, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, out=out)
+    want = loops.head_merge(src_gpu.cpu(), cfg.T, cfg.H, cfg.D, cfg.P, cfg.C)
+    assert same_bits(out.contiguous(), want), first_mismatch(out.contiguous(), want)
+
+
+def test_tiny_iota_bijection():
+    cfg = W.CONFIGS["tiny"]
+    src, _ = W.pack_source(cfg, payload="iota")
+    got = vf.qkv_pack(src.to(DEV), cfg.P, cfg.C).cpu()
+    assert torch.equal(got, loops.qkv_pack(src, cfg.P, cfg.C))
+    n = got.numel()
+    assert torch.equal((got.to(torch.int32) & 0xFFFF).sort().values,
+                       torch.arange(n, dtype=torch.int32))
+
+
+# --------------------------------------------------------------------------
+# Edge cases and degenerate shapes
+# --------------------------------------------------------------------------
+
+def rand_bits(shape, seed, device=DEV):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    t = torch.randint(-(1 << 15), 1 << 15, shape, generator=g, dtype=torch.int32)
+    return t.to(torch.int16).to(device)
+
+
+EDGE_SHAPES = [
+    (0, 4, 8, 2, 4),        # no tokens
+    (1, 4, 8, 2, 4),        # one token, three empty chunks
+    (3, 4, 8, 2, 8),        # C > T
+    (17, 2, 8, 2, 3),       # one head per slot
+    (33, 6, 16, 1, 1),      # P = 1, C = 1
+    (29, 8, 24, 4, 5),      # D = 24 (three 16-byte vectors per head row)
+    (31, 4, 5, 2, 3),       # odd D: scalar path
+    (9, 2, 1, 2, 2),        # D = 1
+    (13, 16, 8, 16, 8),     # P * C = 128 pieces: several launches
+    (5, 4, 4096, 2, 2),     # long head rows: one block row spans 512 vectors
+    (3, 2, 8192, 2, 1),     # head rows longer than one block: d chunks
+    (7, 1024, 8, 2, 2),     # many heads per row: head chunks
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES)
+def test_edges_all_ops(shape):
+    T, H, D, P, C = shape
+    x4 = rand_bits((T, 3, H, D), 1)
+    got = vf.qkv_pack(x4, P, C)
+    assert same_bits(got, loops.qkv_pack(x4.cpu(), P, C))
+    x3 = rand_bits((T, H, D), 2)
+    got = vf.attn_split(x3, P, C)
+    assert same_bits(got, loops.attn_split(x3.cpu(), P, C))
+    flat = rand_bits((T * H * D,), 3)
+    got = vf.head_merge(flat, T, H, D, P, C)
+    assert same_bits(got, loops.head_merge(flat.cpu(), T, H, D, P, C))
+
+
+@pytest.mark.parametrize("P", [1, 3, 7, 64])
+def test_split_more_destinations_than_tokens(P):
+    T, H, D, C = 5, 3, 16, 4
+    x3 = rand_bits((T, H, D), P)
+    got = vf.attn_split(x3, P, C)
+    assert same_bits(got, loops.attn_split(x3.cpu(), P, C))
+
+
+# Element offsets into a bigger allocation select the vector width:
+# offset 0 -> 16-byte vectors, 4 -> 8 bytes, 2 -> 4 bytes, 1 -> 2 bytes.
+@pytest.mark.parametrize("offset", [0, 1, 2, 4])
+def test_alignment_classes(offset):
+    T, H, D, P, C = 37, 4, 32, 2, 3
+    n4 = T * 3 * H * D
+    buf = rand_bits((n4 + 16,), 5)
+    x4 = buf[offset:offset + n4].view(T, 3, H, D)
+    outbuf = torch.zeros(n4 + 16, dtype=torch.int16, device=DEV)
+    out = outbuf[offset:offset + n4]
+    vf.qkv_pack(x4, P, C, out=out)
+    assert same_bits(out, loops.qkv_pack(x4.cpu(), P, C))
+    assert not bool(outbuf[:offset].any()) and not bool(outbuf[offset + n4:].any())
+
+    n3 = T * H * D
+    x3 = buf[offset:offset + n3].view(T, H, D)
+    out = outbuf[offset:offset + n3]
+    vf.attn_split(x3, P, C, out=out)
+    assert same_bits(out, loops.attn_split(x3.cpu(), P, C))
+
+    src = buf[offset:offset + n3]
+    outbuf.zero_()
+    dst = outbuf[offset:offset + n3].view(T, H, D)
+    vf.head_merge(src, T, H, D, P, C, out=dst)
+    assert same_bits(dst, loops.head_merge(src.cpu(), T, H, D, P, C))
+    assert not bool(outbuf[:offset].any()) and not bool(outbuf[offset + n3:].any())
+
+
+@pytest.mark.parametrize("kind", ["padded", "head_major", "d_stride2", "odd_row_stride",
+                                  "zero_stride"])
+def test_strided_sources(kind):
+    T, H, D, P, C = 41, 6, 16, 3, 4
+    if kind == "padded":
+        base = rand_bits((T, 3 * H * D + 24), 6)
+        x4 = base[:, :3 * H * D].unflatten(1, (3, H, D))
+        base3 = rand_bits((T, H * D + 8), 7)
+        x3 = base3[:, :H * D].unflatten(1, (H, D))
+    elif kind == "head_major":
+        x4 = rand_bits((T, H, 3, D), 6).permute(0, 2, 1, 3)
+        x3 = rand_bits((H, T, D), 7).permute(1, 0, 2)
+    elif kind == "d_stride2":
+        x4 = rand_bits((T, 3, H, 2 * D), 6)[..., ::2]
+        x3 = rand_bits((T, H, 2 * D), 7)[..., ::2]
+    elif kind == "odd_row_stride":
+        base = rand_bits((T, 3 * H * D + 3), 6)
+        x4 = base[:, :3 * H * D].unflatten(1, (3, H, D))
+        base3 = rand_bits((T, H * D + 1), 7)
+        x3 = base3[:, :H * D].unflatten(1, (H, D))
+    else:  # every token reads the same row: a broadcast view is a valid source
+        x4 = rand_bits((1, 3, H, D), 6).expand(T, 3, H, D)
+        x3 = rand_bits((1, H, D), 7).expand(T, H, D)
+    assert same_bits(vf.qkv_pack(x4, P, C), loops.qkv_pack(x4.cpu(), P, C))
+    assert same_bits(vf.attn_split(x3, P, C), loops.attn_split(x3.cpu(), P, C))
+
+
+@pytest.mark.parametrize("kind", ["head_major", "padded", "d_stride2"])
+def test_strided_merge_destinations(kind):
+    T, H, D, P, C = 23, 8, 16, 4, 3
+    flat = rand_bits((T * H * D,), 9)
+    if kind == "head_major":
+        big = torch.zeros((H, T, D), dtype=torch.int16, device=DEV)
+        out = big.permute(1, 0, 2)
+    elif kind == "padded":
+        big = torch.zeros((T, H * D + 40), dtype=torch.int16, device=DEV)
+        out = big[:, :H * D].unflatten(1, (H, D))
+    else:
+        big = torch.zeros((T, H, 2 * D), dtype=torch.int16, device=DEV)
+        out = big[..., ::2]
+    vf.head_merge(flat, T, H, D, P, C, out=out)
+    assert same_bits(out.contiguous(), loops.head_merge(flat.cpu(), T, H, D, P, C))
+    if kind == "padded":
+        assert not bool(big[:, H * D:].any())
+    if kind == "d_stride2":
+        assert not bool(big[..., 1::2].any())
+
+
+def test_guard_bands_untouched():
+    cfg = W.CONFIGS["4k"]
+    T, H, D, P, C = cfg.T, cfg.H, cfg.D, cfg.P, cfg.C
+    src, _ = W.pack_source(cfg, device=DEV)
+    n = 3 * T * H * D
+    guard = 4096
+    canary = W._as_i16(0xDEAD)
+    buf = torch.full((n + 2 * guard,), canary, dtype=torch.int16, device=DEV)
+    vf.qkv_pack(src, P, C, out=buf[guard:guard + n])
+    assert bool((buf[:guard] == canary).all()) and bool((buf[guard + n:] == canary).all())
+    assert same_bits(buf[guard:guard + n], loops.qkv_pack(src.cpu(), P, C))
+
+
+def test_non_default_stream_and_no_allocation():
+    cfg = W.CONFIGS["4k"]
+    src, _ = W.pack_source(cfg, device=DEV)
+    out = torch.empty(3 * cfg.T * cfg.H * cfg.D, dtype=torch.int16, device=DEV)
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_allocated(DEV)
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        vf.qkv_pack(src, cfg.P, cfg.C, out=out)
+    torch.cuda.current_stream(DEV).wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(DEV) == before
+    assert same_bits(out, loops.qkv_pack(src.cpu(), cfg.P, cfg.C))
+
+
+def test_rejections_do_not_touch_destination():
+    x4 = rand_bits((8, 3, 4, 8), 1)
+    out = torch.zeros(3 * 8 * 4 * 8, dtype=torch.int16, device=DEV)
+    with pytest.raises(vf.VFError) as e:
+        vf.qkv_pack(x4, 3, 2, out=out)           # H % P != 0
+    assert e.value.status == -1
+    with pytest.raises(vf.VFError) as e:        # destination aliases the source
+        vf.qkv_pack(x4, 2, 2, out=x4.reshape(-1))
+    assert e.value.status == -3
+    merged = torch.zeros(1, dtype=torch.int16, device=DEV).expand(8, 4, 8)
+    with pytest.raises(vf.VFError):             # overlapping destination view
+        vf.head_merge(out[:8 * 4 * 8], 8, 4, 8, 2, 2, out=merged)
+    torch.cuda.synchronize()
+    assert not bool(out.any())
+
+
+def test_host_memory_is_rejected():
+    x4 = torch.zeros((4, 3, 2, 8), dtype=torch.int16)      # pageable host memory
+    out = torch.zeros(3 * 4 * 2 * 8, dtype=torch.int16, device=DEV)
+    rc = vf.lib().vf_qkv_pack(x4.data_ptr(), (vf._I64 * 4)(*x4.stride()), 4, 2, 8, 2, 1,
+                              out.data_ptr(), None)
+    assert rc == -1
