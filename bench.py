@@ -43,7 +43,7 @@ WORKLOAD = "pages"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["sequence_head_relayout_gb300/csrc/relayout_kernel.cuh",
                   "sequence_head_relayout_gb300/csrc/vf_relayout.cu"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic_pages.txt")
 
 
 def kernel_source_hash() -> str:
@@ -52,6 +52,21 @@ def kernel_source_hash() -> str:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """Maximum of a per-rank scalar over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the bytes every rank moved over the slowest rank's time."""
+    return world * steps * bytes_per_rank_step / (max_ms / 1e3) / 1e9
 
 
 def op_elements(cfg):
@@ -227,15 +242,21 @@ def measured_peak():
 
 
 def recorded_traffic():
-    """ncu DRAM bytes per launch for the current kernel source, else None."""
+    """ncu DRAM bytes per launch (read + write) recorded for the current kernel
+    source, as {op: bytes}; None when absent or taken on other kernel code."""
+    d = {}
     try:
         with open(TRAFFIC_FILE) as f:
-            d = json.load(f)
-    except (OSError, ValueError):
+            for line in f:
+                if line.startswith("#") or ":" not in line:
+                    continue
+                k, _, v = line.partition(":")
+                d[k.strip()] = v.strip()
+    except OSError:
         return None
     if d.get("kernel_source_sha") != kernel_source_hash():
         return None
-    return d
+    return {k: int(v) for k, v in d.items() if k in ("qkv_pack", "attn_split", "head_merge")}
 
 
 def make_set(cfg, dev, seed_shift, ops=("qkv_pack", "attn_split", "head_merge")):
@@ -333,14 +354,11 @@ def gpu_arm(args, rank, world, local_rank):
         for j, name in enumerate(ops_run):
             per_op_ms[name].append(e[j].elapsed_time(e[j + 1]))
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = max_over_ranks(total_ms, dev)
 
     elems = op_elements(cfg)
     step_bytes = sum(alg_bytes(elems[n]) for n in ops_run)
-    value = world * K * step_bytes / (max_ms / 1e3) / 1e9
+    value = job_gbs(step_bytes, K, world, max_ms)
     peak, peak_kind = measured_peak()
 
     ops = {}
