@@ -67,3 +67,23 @@ def head_merge(packed: torch.Tensor, T: int, H: int, D: int, P: int, C: int) -> 
         off += n
     assert off == flat.numel()
     return torch.cat(pieces, 0).contiguous()
+
+
+def qkv_unpack_recv(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int):
+    """Receive side of the forward exchange: cut the received storage into
+    (chunk, source rank) blocks, view each as [3, tokens, Hp, D], concatenate
+    each rank's chunks, then the ranks in order -> (Q, K, V) as [T, Hp, D]."""
+    flat = _bits(recv).reshape(-1)
+    Hp = H // P
+    shard = part_sizes(T, P)
+    per_rank = [[] for _ in range(P)]
+    off = 0
+    for c in range(C):
+        for r in range(P):
+            L = part_sizes(shard[r], C)[c]
+            n = 3 * L * Hp * D
+            per_rank[r].append(flat[off:off + n].view(3, L, Hp, D))
+            off += n
+    assert off == flat.numel()
+    full = torch.cat([torch.cat(blocks, 1) for blocks in per_rank], 1)   # [3, T, Hp, D]
+    return tuple(full[s].contiguous() for s in range(3))

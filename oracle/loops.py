@@ -12,7 +12,7 @@ import torch
 
 from . import build as _build
 
-OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE = 0, 1, 2
+OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE, OP_QKV_UNPACK = 0, 1, 2, 3
 
 _lib = None
 _I64 = ctypes.c_int64
@@ -31,6 +31,7 @@ def lib():
             "oracle_attn_unsplit": [_P, _I64, _I64, _I64, _I64, _I64, _P, arr4],
             "oracle_head_merge": [_P, _I64, _I64, _I64, _I64, _I64, _P, arr4],
             "oracle_head_split": [_P, arr4, _I64, _I64, _I64, _I64, _I64, _P],
+            "oracle_qkv_unpack_recv": [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, arr4],
             "oracle_piece_table": [ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
                                    arr4, arr4, arr4, _I64],
         }.items():
@@ -122,6 +123,23 @@ def head_split(src: torch.Tensor, P: int, C: int) -> torch.Tensor:
     n = lib().oracle_head_split(s.data_ptr(), _strides(s), T, H, D, P, C, out.data_ptr())
     _check(n, out.numel(), "head_split")
     return out
+
+
+def qkv_unpack_recv(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
+                    outs=None):
+    """Receive-side QKV unpack: flat received storage of 3*T*(H/P)*D elements
+    into (Q, K, V), each a [T, H/P, D] tensor.  ``outs`` may give three
+    strided [T, H/P, D] int16 views sharing one stride tuple."""
+    r = _bits(recv).contiguous()
+    Hp = H // P
+    if outs is None:
+        outs = tuple(torch.empty((T, Hp, D), dtype=torch.int16) for _ in range(3))
+    q, k, v = (_bits(o) for o in outs)
+    assert q.stride() == k.stride() == v.stride()
+    n = lib().oracle_qkv_unpack_recv(r.data_ptr(), T, H, D, P, C, q.data_ptr(), k.data_ptr(),
+                                     v.data_ptr(), _strides(q))
+    _check(n, 3 * T * Hp * D, "qkv_unpack_recv")
+    return outs
 
 
 def piece_table(op: int, T: int, H: int, D: int, P: int, C: int):

@@ -125,6 +125,40 @@ int64_t oracle_qkv_unpack(const uint16_t *packed,
     return k;
 }
 
+/*
+ * Receive-side QKV unpack ("速度、显存与质量", section "剖析单次去噪请求": the
+ * QKV unpack between the inbound exchange and Flash-SDPA).  Reading: after the
+ * exchange, the rank that owns head group p holds, for each chunk c and each
+ * source rank r (r = 0..P-1), the pack block (c, p) that rank r produced from
+ * its own token shard (shard r of the T global tokens, quota ceil(T/P), cut
+ * into chunks with quota ceil(n_r/C)): [s][token][head-in-group][d].  The
+ * unpack writes Q, K and V as [T][Hp][D] tensors (Hp = H/P) in global token
+ * order, each through the element strides ot[0..2] (token, head, d).
+ */
+int64_t oracle_qkv_unpack_recv(const uint16_t *recv,
+                               int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                               uint16_t *q, uint16_t *k_out, uint16_t *v,
+                               const int64_t ot[3]) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0) return -1;
+    const int64_t Hp = H / P;
+    uint16_t *outs[3] = {q, k_out, v};
+    int64_t k = 0;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t r = 0; r < P; ++r) {
+            const int64_t a = part_begin(T, P, r);             /* shard of rank r */
+            const int64_t n = part_end(T, P, r) - a;
+            const int64_t u0 = part_begin(n, C, c), u1 = part_end(n, C, c);
+            for (int64_t s = 0; s < 3; ++s)
+                for (int64_t u = u0; u < u1; ++u) {
+                    const int64_t t = a + u;
+                    for (int64_t hh = 0; hh < Hp; ++hh)
+                        for (int64_t d = 0; d < D; ++d)
+                            outs[s][t * ot[0] + hh * ot[1] + d * ot[2]] = recv[k++];
+                }
+        }
+    return k;
+}
+
 /* ---- attention-result split -------------------------------------------- */
 
 /*
@@ -236,7 +270,8 @@ int64_t oracle_head_split(const uint16_t *src, const int64_t st[3],
  * token count and the element offset of the block in packed storage,
  * obtained by advancing a cursor over the blocks in the same order as the
  * oracles above.
- * op: 0 = QKV pack, 1 = attention-result split, 2 = returned-head merge.
+ * op: 0 = QKV pack, 1 = attention-result split, 2 = returned-head merge,
+ * 3 = receive-side QKV unpack (entry (c, r): the block from source rank r).
  * Returns the number of entries (C*P), or -1 on bad arguments or cap.
  */
 int64_t oracle_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
@@ -244,16 +279,17 @@ int64_t oracle_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, i
                            int64_t cap) {
     if (bad_dims(T, H, D, P, C) || cap < P * C) return -1;
     if (op != 1 && H % P != 0) return -1;
+    if (op < 0 || op > 3) return -1;
     int64_t k = 0, e = 0;
     for (int64_t c = 0; c < C; ++c)
         for (int64_t p = 0; p < P; ++p, ++e) {
             int64_t first, count, per_token;
-            if (op == 1) {
+            if (op == 1 || op == 3) {
                 const int64_t a = part_begin(T, P, p);
                 const int64_t n = part_end(T, P, p) - a;
                 first = a + part_begin(n, C, c);
                 count = part_end(n, C, c) - part_begin(n, C, c);
-                per_token = H * D;
+                per_token = op == 1 ? H * D : 3 * (H / P) * D;
             } else if (op == 0 || op == 2) {
                 first = part_begin(T, C, c);
                 count = part_end(T, C, c) - first;

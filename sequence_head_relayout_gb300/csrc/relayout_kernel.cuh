@@ -30,9 +30,18 @@
 
 namespace vf {
 
-constexpr int kMaxPieces = 64;       // pieces per launch (kernel parameter space)
-constexpr int kRowsPerThread = 4;    // independent loads in flight per thread
-constexpr int kMaxThreads = 512;     // threads per block, upper bound
+// Launch-shape constants; the defaults were chosen by measurement on GB300 and
+// can be overridden at compile time for tuning sweeps.
+#ifndef VF_ROWS_PER_THREAD
+#define VF_ROWS_PER_THREAD 4
+#endif
+#ifndef VF_CACHE_HINT
+#define VF_CACHE_HINT 0
+#endif
+
+constexpr int kMaxPieces = 64;                     // pieces per launch (parameter space)
+constexpr int kRowsPerThread = VF_ROWS_PER_THREAD; // independent loads in flight per thread
+constexpr int kMaxThreads = 512;                   // threads per block, upper bound
 
 struct Piece {
     int64_t packed_off;    // element offset of the block in packed storage
@@ -62,16 +71,27 @@ template <> struct Vec<4> { using T = uint2; };
 template <> struct Vec<2> { using T = unsigned int; };
 template <> struct Vec<1> { using T = unsigned short; };
 
-// Every element is touched exactly once: read through the read-only path
-// without allocating in L1, and store with the streaming (evict-first) hint.
+// Every element is touched exactly once.  Hint 0: streaming loads and
+// stores (evict-first, `.cs`); 1: read-only path loads (`.nc`), plain stores;
+// 2: plain loads and stores.
 template <typename V>
 __device__ __forceinline__ V load_once(const uint16_t *p) {
+#if VF_CACHE_HINT == 0
     return __ldcs(reinterpret_cast<const V *>(p));
+#elif VF_CACHE_HINT == 1
+    return __ldg(reinterpret_cast<const V *>(p));
+#else
+    return *reinterpret_cast<const V *>(p);
+#endif
 }
 
 template <typename V>
 __device__ __forceinline__ void store_once(uint16_t *p, const V &v) {
+#if VF_CACHE_HINT == 0
     __stcs(reinterpret_cast<V *>(p), v);
+#else
+    *reinterpret_cast<V *>(p) = v;
+#endif
 }
 
 // Grid: x = groups of kRowsPerThread * blockDim.z rows, y = piece,

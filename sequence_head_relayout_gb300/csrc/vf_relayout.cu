@@ -21,7 +21,10 @@
 
 namespace {
 
-constexpr int kTargetThreads = 256;
+#ifndef VF_TARGET_THREADS
+#define VF_TARGET_THREADS 256
+#endif
+constexpr int kTargetThreads = VF_TARGET_THREADS;   // block size aimed at when rows are short
 constexpr int64_t kMaxTablePieces = int64_t(1) << 20;   // P * C limit
 constexpr int64_t kMaxGridZ = 65535;
 constexpr int64_t kMaxTokens = int64_t(1) << 30;

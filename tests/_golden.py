@@ -22,7 +22,8 @@ def load(name: str) -> dict:
             except ValueError:
                 out[key.strip()] = val.strip()
                 continue
-            out[key.strip()] = nums[0] if len(nums) == 1 and key.strip() != "expected" else nums
+            k = key.strip()
+            out[k] = nums[0] if len(nums) == 1 and not k.startswith("expected") else nums
     return out
 
 

@@ -355,3 +355,106 @@ def test_pins_catch_planted_split_mistake():
     g = _golden.load("split_T5_H2_D2_P2_C2.txt")
     src = iota((g["T"], g["H"], g["D"]))
     assert split_global_quota(src, g["P"], g["C"]).tolist() != g["expected"]
+
+
+# --------------------------------------------------------------------------
+# 9. Receive-side QKV unpack
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", _golden.examples("unpack"))
+def test_golden_unpack(name):
+    g = _golden.load(name)
+    T, H, D, P, C = g["T"], g["H"], g["D"], g["P"], g["C"]
+    recv = iota((3 * T * (H // P) * D,))
+    for impl in (loops.qkv_unpack_recv, chain.qkv_unpack_recv):
+        q, k, v = impl(recv, T, H, D, P, C)
+        assert q.reshape(-1).tolist() == g["expected_q"]
+        assert k.reshape(-1).tolist() == g["expected_k"]
+        assert v.reshape(-1).tolist() == g["expected_v"]
+
+
+def forward_exchange(X: torch.Tensor, P: int, C: int):
+    """Ulysses forward path on P virtual ranks, on CPU: rank r packs its token
+    shard of the global [T,3,H,D] activation; block (c, p) of rank r travels to
+    rank p, which stores it at source slot r of its chunk-c block."""
+    T, _, H, D = X.shape
+    shard = -(-T // P)
+    bounds = [(min(T, r * shard), min(T, (r + 1) * shard)) for r in range(P)]
+    sent, tables = [], []
+    for a, b in bounds:
+        sent.append(loops.qkv_pack(X[a:b], P, C))
+        tables.append(loops.piece_table(loops.OP_QKV_PACK, b - a, H, D, P, C))
+    recv = []
+    for p in range(P):
+        parts = []
+        for c in range(C):
+            for r in range(P):
+                e = c * P + p
+                length, off = tables[r][1][e], tables[r][2][e]
+                parts.append(sent[r][off:off + 3 * length * (H // P) * D])
+        recv.append(torch.cat(parts))
+    return recv
+
+
+@pytest.mark.parametrize("shape", [(37, 8, 4, 2, 4), (55, 12, 2, 4, 4), (5, 4, 2, 4, 2),
+                                   (64, 4, 16, 2, 1), (9, 6, 3, 3, 5)])
+def test_virtual_exchange_pack_then_unpack(shape):
+    T, H, D, P, C = shape
+    X = rand_bits((T, 3, H, D), 21)
+    Hp = H // P
+    for p, recv in enumerate(forward_exchange(X, P, C)):
+        q, k, v = loops.qkv_unpack_recv(recv, T, H, D, P, C)
+        for s, out in enumerate((q, k, v)):
+            assert bits_equal(out, X[:, s, p * Hp:(p + 1) * Hp].contiguous()), (p, s)
+
+
+def test_unpack_library_reduction():
+    T, H, D = 11, 6, 4
+    recv = rand_bits((3 * T * H * D,), 5)
+    q, k, v = loops.qkv_unpack_recv(recv, T, H, D, 1, 1)
+    ref = recv.view(3, T, H, D)
+    for s, out in enumerate((q, k, v)):
+        assert bits_equal(out, ref[s])
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_unpack_loops_agree_with_chain(shape):
+    T, H, D, P, C = shape
+    recv = rand_bits((3 * T * (H // P) * D,), 31)
+    want = chain.qkv_unpack_recv(recv, T, H, D, P, C)
+    # strided outputs: [H/P, T, D] allocations viewed as [T, H/P, D]
+    outs = tuple(torch.zeros((H // P, T, D), dtype=torch.int16).permute(1, 0, 2)
+                 for _ in range(3))
+    got = loops.qkv_unpack_recv(recv, T, H, D, P, C, outs=outs)
+    for a, b in zip(got, want):
+        assert bits_equal(a.contiguous(), b)
+
+
+def test_unpack_iota_bijection():
+    T, H, D, P, C = 13, 8, 3, 4, 3
+    n = 3 * T * (H // P) * D
+    out = torch.cat([o.reshape(-1) for o in loops.qkv_unpack_recv(iota((n,)), T, H, D, P, C)])
+    assert torch.equal(out.to(torch.int32).sort().values, torch.arange(n, dtype=torch.int32))
+
+
+def test_pins_catch_planted_unpack_mistake():
+    # chunking every source rank's shard with the global quota ceil(T/C)
+    def unpack_global_quota(recv, T, H, D, P, C):
+        flat = recv.reshape(-1)
+        Hp = H // P
+        q = -(-T // C)
+        shard = chain.part_sizes(T, P)
+        per_rank = [[] for _ in range(P)]
+        off = 0
+        for c in range(C):
+            for r in range(P):
+                L = max(0, min(q, shard[r] - c * q))
+                n = 3 * L * Hp * D
+                per_rank[r].append(flat[off:off + n].view(3, L, Hp, D))
+                off += n
+        full = torch.cat([torch.cat(b, 1) for b in per_rank], 1)
+        return tuple(full[s].contiguous() for s in range(3))
+    g = _golden.load("unpack_T5_H4_D1_P2_C2.txt")
+    recv = iota((30,))
+    q, _, _ = unpack_global_quota(recv, 5, 4, 1, 2, 2)
+    assert q.reshape(-1).tolist() != g["expected_q"]
