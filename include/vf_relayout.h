@@ -78,7 +78,8 @@ typedef enum vf_status {
 typedef enum vf_op {
     VF_OP_QKV_PACK = 0,
     VF_OP_ATTN_SPLIT = 1,
-    VF_OP_HEAD_MERGE = 2
+    VF_OP_HEAD_MERGE = 2,
+    VF_OP_QKV_UNPACK = 3
 } vf_op;
 
 /*
@@ -142,17 +143,79 @@ int vf_head_merge(const void *src, const int64_t dst_strides[3],
                   void *dst, vf_stream_t stream);
 
 /*
+ * Receive-side QKV unpack.  ("速度、显存与质量", section "剖析单次去噪请求": the
+ * QKV unpack between the inbound exchange and Flash-SDPA; it inverts the
+ * pack of "Sol-Engine alignment on SM86 and SM89", "What is enabled", across
+ * the all-to-all.)
+ *
+ * Shapes are the global ones: T tokens over all ranks, H heads in total,
+ * P ranks; this rank owns one head group of Hp = H/P heads.  Source rank r
+ * owned token shard r (quota ceil(T/P)) and packed it with chunk quota
+ * ceil(n_r/C).
+ * recv:        3*T*Hp*D contiguous elements as received: for each chunk c,
+ *              for each source rank r, that rank's pack block for this head
+ *              group, [s][L][Hp][D] (s = q, k, v).
+ * q, k, v:     three [T][Hp][D] views written once, in global token order,
+ *              all with the element strides out_strides[3] (token, head, d),
+ *              or NULL for contiguous (Hp*D, D, 1).  Each view must not
+ *              overlap itself, the others or recv.
+ * Requires H % P == 0.
+ */
+int vf_qkv_unpack(const void *recv, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                  void *q, void *k, void *v, const int64_t out_strides[3],
+                  vf_stream_t stream);
+
+/*
+ * Chunk-range variants for the overlap pipeline ("Sol-Engine alignment on
+ * SM86 and SM89", "What is enabled": Vflash's four-chunk overlap layout, in
+ * which chunk c's exchange overlaps the relayout of the next chunk).  Each
+ * takes the same arguments as its full form plus chunks
+ * [c_begin, c_begin + c_count) (0 <= c_begin, c_count >= 0,
+ * c_begin + c_count <= C) and moves only those chunks' blocks: the packed
+ * buffer is always the full one and block offsets are those of
+ * vf_piece_table; the strided side is only touched at the chunks' tokens.
+ * c_count == 0 returns VF_OK without touching the GPU.
+ */
+int vf_qkv_pack_chunks(const void *src, const int64_t src_strides[4],
+                       int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                       int64_t c_begin, int64_t c_count, void *dst, vf_stream_t stream);
+int vf_attn_split_chunks(const void *src, const int64_t src_strides[3],
+                         int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                         int64_t c_begin, int64_t c_count, void *dst, vf_stream_t stream);
+int vf_head_merge_chunks(const void *src, const int64_t dst_strides[3],
+                         int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                         int64_t c_begin, int64_t c_count, void *dst, vf_stream_t stream);
+int vf_qkv_unpack_chunks(const void *recv, int64_t T, int64_t H, int64_t D, int64_t P,
+                         int64_t C, int64_t c_begin, int64_t c_count,
+                         void *q, void *k, void *v, const int64_t out_strides[3],
+                         vf_stream_t stream);
+
+/*
+ * QKV destination pack from three separate Q, K, V views (projections that
+ * were not fused into one GEMM; "Sol-Engine alignment on SM86 and SM89",
+ * table "Upstream gap and disposition", row "Merged QKV projection", is the
+ * fused case).  q, k, v: [T][H][D] views sharing the element strides
+ * qkv_strides[3] (token, head, d); they may overlap each other (read only).
+ * Output, chunk range and rules as vf_qkv_pack_chunks: the result equals
+ * vf_qkv_pack of the [T][3][H][D] view whose slabs are q, k, v.
+ */
+int vf_qkv_pack3(const void *q, const void *k, const void *v, const int64_t qkv_strides[3],
+                 int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                 int64_t c_begin, int64_t c_count, void *dst, vf_stream_t stream);
+
+/*
  * Number of elements of the packed side of `op` (3*T*H*D for the pack,
- * T*H*D otherwise), or a negative vf_status on bad arguments or overflow.
- * Pure host function.
+ * T*H*D for the split and the merge, 3*T*(H/P)*D for the unpack), or a
+ * negative vf_status on bad arguments or overflow.  Pure host function.
  */
 int64_t vf_packed_elems(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C);
 
 /*
  * The piece table of `op`: for each (c, p) in storage order (c outer), the
- * first token (tok_start; for the split, counted in the source's token
- * numbering), the token count (tok_len) and the element offset of the block
- * in packed storage (packed_off).  Writes C*P entries into each caller-owned
+ * first token (tok_start; for the split and the unpack, counted in the
+ * strided view's token numbering, so shard p's chunk c), the token count
+ * (tok_len) and the element offset of the block in packed storage
+ * (packed_off).  For the unpack, p is the source rank.  Writes C*P entries into each caller-owned
  * array of capacity `cap` and returns C*P, or a negative vf_status
  * (VF_ERR_CAPACITY when cap < C*P).  Pure host function.
  */

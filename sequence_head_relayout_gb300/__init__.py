@@ -12,17 +12,24 @@ enabled"):
 
 * :func:`qkv_pack`   -- fused [T,3,H,D] QKV view -> destination-major send buffer;
 * :func:`attn_split` -- attention output [T,H,D] view -> per-destination token shards;
-* :func:`head_merge` -- received destination-major buffer -> token-major [T,H,D].
+* :func:`head_merge` -- received destination-major buffer -> token-major [T,H,D];
+* :func:`qkv_unpack` -- received QKV buffer -> Q, K, V [T,H/P,D] views ("速度、显存与
+  质量", section "剖析单次去噪请求": the QKV unpack before Flash-SDPA);
+* :func:`qkv_pack3`  -- the pack from three separate Q, K, V views.
+
+Every function takes ``chunks=(c_begin, c_count)`` to move only those overlap
+chunks (the packed buffer is always the full one).
 """
 import ctypes
 import os
 
 import torch
 
-__all__ = ["qkv_pack", "attn_split", "head_merge", "packed_elems", "piece_table",
-           "VFError", "lib", "OP_QKV_PACK", "OP_ATTN_SPLIT", "OP_HEAD_MERGE"]
+__all__ = ["qkv_pack", "qkv_pack3", "attn_split", "head_merge", "qkv_unpack", "packed_elems",
+           "piece_table", "VFError", "lib", "OP_QKV_PACK", "OP_ATTN_SPLIT", "OP_HEAD_MERGE",
+           "OP_QKV_UNPACK"]
 
-OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE = 0, 1, 2
+OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE, OP_QKV_UNPACK = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libvf_relayout.so")
@@ -50,12 +57,21 @@ def lib():
             raise RuntimeError("libvf_relayout.so is not built; run "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
         l = ctypes.CDLL(LIB_PATH)
-        for name in ("vf_qkv_pack", "vf_attn_split"):
+        sig = {
+            "vf_qkv_pack": [_P, _I64P] + [_I64] * 5 + [_P, _P],
+            "vf_attn_split": [_P, _I64P] + [_I64] * 5 + [_P, _P],
+            "vf_head_merge": [_P, _I64P] + [_I64] * 5 + [_P, _P],
+            "vf_qkv_unpack": [_P] + [_I64] * 5 + [_P, _P, _P, _I64P, _P],
+            "vf_qkv_pack_chunks": [_P, _I64P] + [_I64] * 7 + [_P, _P],
+            "vf_attn_split_chunks": [_P, _I64P] + [_I64] * 7 + [_P, _P],
+            "vf_head_merge_chunks": [_P, _I64P] + [_I64] * 7 + [_P, _P],
+            "vf_qkv_unpack_chunks": [_P] + [_I64] * 7 + [_P, _P, _P, _I64P, _P],
+            "vf_qkv_pack3": [_P, _P, _P, _I64P] + [_I64] * 7 + [_P, _P],
+        }
+        for name, args in sig.items():
             f = getattr(l, name)
-            f.argtypes = [_P, _I64P, _I64, _I64, _I64, _I64, _I64, _P, _P]
+            f.argtypes = args
             f.restype = ctypes.c_int
-        l.vf_head_merge.argtypes = [_P, _I64P, _I64, _I64, _I64, _I64, _I64, _P, _P]
-        l.vf_head_merge.restype = ctypes.c_int
         l.vf_packed_elems.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, _I64]
         l.vf_packed_elems.restype = _I64
         l.vf_piece_table.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
@@ -110,8 +126,21 @@ def piece_table(op: int, T: int, H: int, D: int, P: int, C: int):
     return list(a), list(b), list(c)
 
 
+def _range(chunks, C):
+    return (0, C) if chunks is None else (int(chunks[0]), int(chunks[1]))
+
+
+def _flat_out(out, n, like):
+    if out is None:
+        out = torch.empty(n, dtype=like.dtype, device=like.device)
+    _check16(out, "out")
+    if not out.is_contiguous() or out.numel() != n:
+        raise ValueError("out must be contiguous with %d elements" % n)
+    return out
+
+
 def qkv_pack(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
-             stream: torch.cuda.Stream = None) -> torch.Tensor:
+             stream: torch.cuda.Stream = None, chunks=None) -> torch.Tensor:
     """QKV destination pack of a [T,3,H,D] CUDA view (any strides).
 
     Returns (or fills) a flat tensor of 3*T*H*D elements: blocks (c, p) in
@@ -121,19 +150,33 @@ def qkv_pack(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
     if src.dim() != 4 or src.shape[1] != 3:
         raise ValueError("src must be a [T,3,H,D] view")
     T, _, H, D = src.shape
-    n = packed_elems(OP_QKV_PACK, T, H, D, P, C)
-    if out is None:
-        out = torch.empty(n, dtype=src.dtype, device=src.device)
-    _check16(out, "out")
-    if not out.is_contiguous() or out.numel() != n:
-        raise ValueError("out must be contiguous with %d elements" % n)
-    _call("vf_qkv_pack", src.data_ptr(), _strides(src), T, H, D, P, C, out.data_ptr(),
-          _stream(stream, src.device))
+    out = _flat_out(out, packed_elems(OP_QKV_PACK, T, H, D, P, C), src)
+    c0, cn = _range(chunks, C)
+    _call("vf_qkv_pack_chunks", src.data_ptr(), _strides(src), T, H, D, P, C, c0, cn,
+          out.data_ptr(), _stream(stream, src.device))
+    return out
+
+
+def qkv_pack3(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, C: int,
+              out: torch.Tensor = None, stream: torch.cuda.Stream = None,
+              chunks=None) -> torch.Tensor:
+    """QKV destination pack from three [T,H,D] CUDA views with equal strides."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _check16(t, name)
+    if q.dim() != 3 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must be [T,H,D] views of one shape")
+    if q.stride() != k.stride() or q.stride() != v.stride():
+        raise ValueError("q, k, v must share their strides")
+    T, H, D = q.shape
+    out = _flat_out(out, packed_elems(OP_QKV_PACK, T, H, D, P, C), q)
+    c0, cn = _range(chunks, C)
+    _call("vf_qkv_pack3", q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), T, H, D, P,
+          C, c0, cn, out.data_ptr(), _stream(stream, q.device))
     return out
 
 
 def attn_split(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
-               stream: torch.cuda.Stream = None) -> torch.Tensor:
+               stream: torch.cuda.Stream = None, chunks=None) -> torch.Tensor:
     """Attention-result split of a [T,H,D] CUDA view (any strides).
 
     Returns (or fills) a flat tensor of T*H*D elements: blocks (c, p) in
@@ -143,19 +186,16 @@ def attn_split(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
     if src.dim() != 3:
         raise ValueError("src must be a [T,H,D] view")
     T, H, D = src.shape
-    n = packed_elems(OP_ATTN_SPLIT, T, H, D, P, C)
-    if out is None:
-        out = torch.empty(n, dtype=src.dtype, device=src.device)
-    _check16(out, "out")
-    if not out.is_contiguous() or out.numel() != n:
-        raise ValueError("out must be contiguous with %d elements" % n)
-    _call("vf_attn_split", src.data_ptr(), _strides(src), T, H, D, P, C, out.data_ptr(),
-          _stream(stream, src.device))
+    out = _flat_out(out, packed_elems(OP_ATTN_SPLIT, T, H, D, P, C), src)
+    c0, cn = _range(chunks, C)
+    _call("vf_attn_split_chunks", src.data_ptr(), _strides(src), T, H, D, P, C, c0, cn,
+          out.data_ptr(), _stream(stream, src.device))
     return out
 
 
 def head_merge(src: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
-               out: torch.Tensor = None, stream: torch.cuda.Stream = None) -> torch.Tensor:
+               out: torch.Tensor = None, stream: torch.cuda.Stream = None,
+               chunks=None) -> torch.Tensor:
     """Returned-head merge of a flat received buffer into a [T,H,D] view.
 
     ``out`` may be any non-overlapping strided [T,H,D] CUDA view; a
@@ -170,6 +210,36 @@ def head_merge(src: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
     _check16(out, "out")
     if tuple(out.shape) != (T, H, D):
         raise ValueError("out must have shape [T,H,D]")
-    _call("vf_head_merge", src.data_ptr(), _strides(out), T, H, D, P, C, out.data_ptr(),
-          _stream(stream, src.device))
+    c0, cn = _range(chunks, C)
+    _call("vf_head_merge_chunks", src.data_ptr(), _strides(out), T, H, D, P, C, c0, cn,
+          out.data_ptr(), _stream(stream, src.device))
     return out
+
+
+def qkv_unpack(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int, outs=None,
+               stream: torch.cuda.Stream = None, chunks=None):
+    """Receive-side QKV unpack: flat received buffer of 3*T*(H/P)*D elements
+    into (Q, K, V), each a [T, H/P, D] view (global token order).
+
+    ``outs`` may give three non-overlapping [T, H/P, D] CUDA views sharing one
+    stride tuple; contiguous tensors are allocated when it is omitted.
+    """
+    _check16(recv, "recv")
+    n = packed_elems(OP_QKV_UNPACK, T, H, D, P, C)
+    if not recv.is_contiguous() or recv.numel() != n:
+        raise ValueError("recv must be contiguous with %d elements" % n)
+    Hp = H // P
+    if outs is None:
+        outs = tuple(torch.empty((T, Hp, D), dtype=recv.dtype, device=recv.device)
+                     for _ in range(3))
+    q, k, v = outs
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _check16(t, name)
+        if tuple(t.shape) != (T, Hp, D):
+            raise ValueError("%s must have shape [T,H/P,D]" % name)
+    if q.stride() != k.stride() or q.stride() != v.stride():
+        raise ValueError("q, k, v must share their strides")
+    c0, cn = _range(chunks, C)
+    _call("vf_qkv_unpack_chunks", recv.data_ptr(), T, H, D, P, C, c0, cn, q.data_ptr(),
+          k.data_ptr(), v.data_ptr(), _strides(q), _stream(stream, recv.device))
+    return outs

@@ -1,15 +1,15 @@
 // Device side of the three relayouts: one row-block copy kernel.
 //
-// All three operations ("Sol-Engine alignment on SM86 and SM89", section
+// All the operations ("Sol-Engine alignment on SM86 and SM89", section
 // "What is enabled": QKV destination pack, attention result split,
-// returned-head merge) move whole token rows between a contiguous *packed*
-// side (the exchange buffer, destination-major) and a *strided* side (the
-// caller's tensor view).  The host cuts the work into pieces; a piece is one
-// (chunk, destination) block of the packed storage:
+// returned-head merge; "速度、显存与质量", section "剖析单次去噪请求": the
+// receive-side QKV unpack) move whole token rows between a contiguous
+// *packed* side (the exchange buffer, destination-major) and a *strided*
+// side (the caller's tensor views).  The host cuts the work into pieces; a
+// piece is one (chunk, destination[, q/k/v slab]) block of the packed storage:
 //
-//   packed  : rows x (heads x D) contiguous elements starting at packed_off
-//             (+ slab * rows * heads * D for the pack's q/k/v slabs);
-//   strided : element (row, head, d) at strided_off + slab * slab_stride
+//   packed  : rows x (heads x D) contiguous elements starting at packed_off;
+//   strided : element (row, head, d) at strided
 //             + row * row_stride + head * head_stride + d * d_stride.
 //
 // There is no element-level transpose: the (token, head) interchange between
@@ -39,29 +39,28 @@ namespace vf {
 #define VF_CACHE_HINT 0
 #endif
 
-constexpr int kMaxPieces = 64;                     // pieces per launch (parameter space)
+constexpr int kMaxPieces = 128;                    // pieces per launch (parameter space)
 constexpr int kRowsPerThread = VF_ROWS_PER_THREAD; // independent loads in flight per thread
 constexpr int kMaxThreads = 512;                   // threads per block, upper bound
 
 struct Piece {
     int64_t packed_off;    // element offset of the block in packed storage
-    int64_t strided_off;   // element offset of the block's first row, strided side
+    uint16_t *strided;     // the block's first row on the strided side
     int64_t rows;          // tokens in the block
 };
 
+// Read-only sides are passed through the same (non-const) pointer fields;
+// the kernel only loads from the side it reads.
 struct Args {
-    const uint16_t *src;
-    uint16_t *dst;
+    uint16_t *packed;      // packed storage
     int64_t row_stride;    // strided side, between consecutive rows (tokens)
     int64_t head_stride;   // strided side, between heads of one row
     int64_t d_stride;      // strided side, along d (1 on every vector path)
-    int64_t slab_stride;   // strided side, between the pack's q/k/v slabs
     int32_t heads;         // heads per packed row
     int32_t D;             // elements per head row
     int32_t npieces;
-    int32_t hchunks;       // ceil(heads / blockDim.y)
     int32_t dchunks;       // ceil(D / VW / blockDim.x)
-    int32_t z_base;        // first folded z index of this launch
+    int32_t z_base;        // first folded z index of this launch (head, d chunks)
     Piece pieces[kMaxPieces];
 };
 
@@ -95,7 +94,7 @@ __device__ __forceinline__ void store_once(uint16_t *p, const V &v) {
 }
 
 // Grid: x = groups of kRowsPerThread * blockDim.z rows, y = piece,
-// z = (slab, head chunk, d chunk) folded, offset by z_base.  Block: x = vector
+// z = (head chunk, d chunk) folded, offset by z_base.  Block: x = vector
 // within a head row, y = head, z = row.  A thread copies one vector of each of
 // its kRowsPerThread rows: all loads first, then all stores.
 template <int VW, bool kPackedIsDst>
@@ -106,23 +105,19 @@ relayout_rows(const __grid_constant__ Args a) {
     const int rows = int(pc.rows);
     const int rstep = int(blockDim.z);
     const int row0 = int(blockIdx.x) * (kRowsPerThread * rstep) + int(threadIdx.z);
-    const int per_slab = a.hchunks * a.dchunks;
     const int z = int(blockIdx.z) + a.z_base;
-    const int slab = z / per_slab;                         // block-uniform
-    const int rem = z - slab * per_slab;
-    const int hc = rem / a.dchunks;
+    const int hc = z / a.dchunks;                          // block-uniform
     const int hh = hc * int(blockDim.y) + int(threadIdx.y);
-    const int dx = (rem - hc * a.dchunks) * int(blockDim.x) + int(threadIdx.x);
+    const int dx = (z - hc * a.dchunks) * int(blockDim.x) + int(threadIdx.x);
     if (row0 >= rows || hh >= a.heads || dx * VW >= a.D) return;
 
     const int64_t R = int64_t(a.heads) * a.D;              // packed row length
-    const int64_t po = pc.packed_off + int64_t(slab) * rows * R + int64_t(row0) * R
-                     + int64_t(hh) * a.D + int64_t(dx) * VW;
-    const int64_t so = pc.strided_off + int64_t(slab) * a.slab_stride
-                     + int64_t(row0) * a.row_stride + int64_t(hh) * a.head_stride
+    const int64_t po = pc.packed_off + int64_t(row0) * R + int64_t(hh) * a.D
+                     + int64_t(dx) * VW;
+    const int64_t so = int64_t(row0) * a.row_stride + int64_t(hh) * a.head_stride
                      + int64_t(dx) * VW * a.d_stride;
-    const uint16_t *s = a.src + (kPackedIsDst ? so : po);
-    uint16_t *d = a.dst + (kPackedIsDst ? po : so);
+    const uint16_t *s = kPackedIsDst ? pc.strided + so : a.packed + po;
+    uint16_t *d = kPackedIsDst ? a.packed + po : pc.strided + so;
     const int64_t s_step = int64_t(rstep) * (kPackedIsDst ? a.row_stride : R);
     const int64_t d_step = int64_t(rstep) * (kPackedIsDst ? R : a.row_stride);
 

@@ -7,13 +7,16 @@
 // chunk quota Q(n) = ceil(n/C) with a short tail; packed storage is blocks
 // (c, p), c outer; the pack's block carries head group p as q, k, v slabs;
 // the split cuts tokens into P shards of ceil(T/P) and each shard into C
-// chunks of ceil(n_p/C); the merge is the inverse of a head-group split.
+// chunks of ceil(n_p/C); the merge is the inverse of a head-group split; the
+// receive-side unpack ("速度、显存与质量", section "剖析单次去噪请求": QKV
+// unpack) reads, per chunk, the pack blocks of the P source ranks' shards.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <utility>
 #include <vector>
 
 #include "relayout_kernel.cuh"
@@ -47,21 +50,36 @@ struct Shape {
     int64_t T, H, D, P, C;
 };
 
+bool is_op(int op) { return op >= VF_OP_QKV_PACK && op <= VF_OP_QKV_UNPACK; }
+
+// Pack and unpack move q, k and v slabs.
+int64_t slabs_of(int op) { return (op == VF_OP_QKV_PACK || op == VF_OP_QKV_UNPACK) ? 3 : 1; }
+
 int check_shape(const Shape &s) {
-    if (s.op < VF_OP_QKV_PACK || s.op > VF_OP_HEAD_MERGE) return VF_ERR_ARG;
+    if (!is_op(s.op)) return VF_ERR_ARG;
     if (s.T < 0 || s.H < 0 || s.D < 0 || s.P < 1 || s.C < 1) return VF_ERR_ARG;
-    if (s.T > kMaxTokens) return VF_ERR_ARG;          // row indices stay in int32
+    if (s.T > kMaxTokens) return VF_ERR_ARG;           // row indices stay in int32
     if (s.op != VF_OP_ATTN_SPLIT && s.H % s.P != 0) return VF_ERR_ARG;
     int64_t n, pc;
     if (!mul_ok(s.T, s.H, &n) || !mul_ok(n, s.D, &n)) return VF_ERR_OVERFLOW;
-    if (s.op == VF_OP_QKV_PACK && !mul_ok(n, 3, &n)) return VF_ERR_OVERFLOW;
-    if (!mul_ok(n, 2, &n)) return VF_ERR_OVERFLOW;            // bytes
+    if (!mul_ok(n, 3, &n) || !mul_ok(n, 2, &n)) return VF_ERR_OVERFLOW;   // bytes, with slabs
     if (!mul_ok(s.P, s.C, &pc) || pc > kMaxTablePieces) return VF_ERR_ARG;
     return VF_OK;
 }
 
+// Elements of the packed side.
 int64_t packed_elems(const Shape &s) {
-    return s.T * s.H * s.D * (s.op == VF_OP_QKV_PACK ? 3 : 1);
+    const int64_t thd = s.T * s.H * s.D;
+    switch (s.op) {
+        case VF_OP_QKV_PACK: return 3 * thd;
+        case VF_OP_QKV_UNPACK: return 3 * thd / s.P;
+        default: return thd;
+    }
+}
+
+// Heads in one packed row.
+int64_t heads_per_row(const Shape &s) {
+    return s.op == VF_OP_ATTN_SPLIT ? s.H : s.H / s.P;
 }
 
 // One (c, p) entry of the piece table.
@@ -70,32 +88,30 @@ struct Entry {
 };
 
 // Piece table in storage order (c outer, p inner).  Requires check_shape OK.
+// Pack and merge cut the T tokens of this rank into chunks; the split and the
+// unpack cut T into P token shards first and each shard into chunks.
 std::vector<Entry> piece_table(const Shape &s) {
     std::vector<Entry> out;
     out.reserve(size_t(s.P * s.C));
+    const int64_t per_token = slabs_of(s.op) * heads_per_row(s) * s.D;
+    const bool sharded = s.op == VF_OP_ATTN_SPLIT || s.op == VF_OP_QKV_UNPACK;
     int64_t cursor = 0;                                     // packed elements
-    if (s.op == VF_OP_ATTN_SPLIT) {
-        const int64_t per_token = s.H * s.D;
-        for (int64_t c = 0; c < s.C; ++c)
-            for (int64_t p = 0; p < s.P; ++p) {
+    for (int64_t c = 0; c < s.C; ++c)
+        for (int64_t p = 0; p < s.P; ++p) {
+            int64_t first, len;
+            if (sharded) {
                 const int64_t a = part_begin(s.T, s.P, p);
                 const int64_t n = part_begin(s.T, s.P, p + 1) - a;
                 const int64_t u0 = part_begin(n, s.C, c);
-                const int64_t len = part_begin(n, s.C, c + 1) - u0;
-                out.push_back({a + u0, len, cursor});
-                cursor += len * per_token;
+                first = a + u0;
+                len = part_begin(n, s.C, c + 1) - u0;
+            } else {
+                first = part_begin(s.T, s.C, c);
+                len = part_begin(s.T, s.C, c + 1) - first;
             }
-    } else {
-        const int64_t per_token = (s.op == VF_OP_QKV_PACK ? 3 : 1) * (s.H / s.P) * s.D;
-        for (int64_t c = 0; c < s.C; ++c) {
-            const int64_t t0 = part_begin(s.T, s.C, c);
-            const int64_t len = part_begin(s.T, s.C, c + 1) - t0;
-            for (int64_t p = 0; p < s.P; ++p) {
-                out.push_back({t0, len, cursor});
-                cursor += len * per_token;
-            }
+            out.push_back({first, len, cursor});
+            cursor += len * per_token;
         }
-    }
     return out;
 }
 
@@ -130,10 +146,15 @@ bool non_overlapping(const int64_t *ext, const int64_t *str, int nd) {
     return true;
 }
 
-// Byte ranges [a, a + na) and [b, b + nb) intersect.
-bool ranges_overlap(uintptr_t a, uint64_t na, uintptr_t b, uint64_t nb) {
-    if (na == 0 || nb == 0) return false;
-    return a < b + nb && b < a + na;
+// A byte range [lo, lo + len).
+struct Range {
+    uintptr_t lo;
+    uint64_t len;
+};
+
+bool overlap(const Range &a, const Range &b) {
+    if (a.len == 0 || b.len == 0) return false;
+    return a.lo < b.lo + b.len && b.lo < a.lo + a.len;
 }
 
 int check_pointer(const void *p) {
@@ -154,13 +175,22 @@ int check_pointer(const void *p) {
     return VF_OK;
 }
 
+// One call, after the entry point has mapped its arguments.
+struct Request {
+    Shape s;
+    int64_t c_begin, c_end;        // chunk range [c_begin, c_end)
+    void *packed;                  // packed storage (read for merge/unpack)
+    const void *strided[3];        // strided-side base per slab
+    int64_t str[3];                // strided view strides (token, head, d), elements
+    int64_t heads_view;            // head extent of the strided view
+    bool strided_written;          // merge, unpack
+};
+
 // Everything one launch family needs besides the pieces.
 struct Plan {
-    const uint16_t *src;
-    uint16_t *dst;
-    bool packed_is_dst;
-    int64_t row_stride, head_stride, d_stride, slab_stride;
-    int64_t heads, D, slabs;
+    uint16_t *packed;
+    int64_t row_stride, head_stride, d_stride;
+    int64_t heads, D;
     std::vector<vf::Piece> pieces;
 };
 
@@ -172,20 +202,17 @@ int launch_family(const Plan &pl, cudaStream_t stream) {
     const int bz = std::max(1, std::min(64, kTargetThreads / (bx * by)));
     const int64_t dchunks = ceil_div(dvec, bx);
     const int64_t hchunks = ceil_div(pl.heads, by);
-    const int64_t zcount = pl.slabs * hchunks * dchunks;   // <= 3 * heads * D
+    const int64_t zcount = hchunks * dchunks;              // <= heads * D
     if (zcount > INT32_MAX) return VF_ERR_ARG;
 
     vf::Args a;
     std::memset(&a, 0, sizeof(a));
-    a.src = pl.src;
-    a.dst = pl.dst;
+    a.packed = pl.packed;
     a.row_stride = pl.row_stride;
     a.head_stride = pl.head_stride;
     a.d_stride = pl.d_stride;
-    a.slab_stride = pl.slab_stride;
     a.heads = int32_t(pl.heads);
     a.D = int32_t(pl.D);
-    a.hchunks = int32_t(hchunks);
     a.dchunks = int32_t(dchunks);
 
     const int64_t rows_per_block = int64_t(vf::kRowsPerThread) * bz;
@@ -227,125 +254,216 @@ int launch_dir(const Plan &pl, int vw, cudaStream_t stream) {
 }
 
 // Widest vector (in elements) that keeps every access of both sides aligned.
-int pick_vector_width(const Plan &pl, const void *packed, const void *strided) {
+int pick_vector_width(const Plan &pl) {
     int64_t max_rows = 0;
     for (const auto &p : pl.pieces) max_rows = std::max(max_rows, p.rows);
     for (int vw : {8, 4, 2}) {
-        const int64_t bytes = 2 * vw;
+        const uintptr_t bytes = uintptr_t(2 * vw);
         if (pl.D % vw != 0) continue;
         if (pl.d_stride != 1) continue;
-        if (reinterpret_cast<uintptr_t>(packed) % bytes) continue;
-        if (reinterpret_cast<uintptr_t>(strided) % bytes) continue;
+        if (reinterpret_cast<uintptr_t>(pl.packed) % bytes) continue;
         if (max_rows > 1 && pl.row_stride % vw) continue;
         if (pl.heads > 1 && pl.head_stride % vw) continue;
-        if (pl.slabs > 1 && pl.slab_stride % vw) continue;
         bool ok = true;
-        for (const auto &p : pl.pieces) ok = ok && (p.strided_off % vw == 0);
+        for (const auto &p : pl.pieces)
+            ok = ok && reinterpret_cast<uintptr_t>(p.strided) % bytes == 0;
         if (ok) return vw;
     }
     return 1;
 }
 
-int run(const Shape &s, const void *src, const int64_t *strides, void *dst, cudaStream_t stream) {
+int run(Request rq, cudaStream_t stream) {
+    const Shape &s = rq.s;
     int rc = check_shape(s);
     if (rc != VF_OK) return rc;
+    if (rq.c_begin < 0 || rq.c_end < rq.c_begin || rq.c_end > s.C) return VF_ERR_ARG;
+    const int64_t slabs = slabs_of(s.op);
 
-    // The strided side's logical extents and strides.
-    int64_t ext[4], str[4];
-    int nd;
-    if (s.op == VF_OP_QKV_PACK) {
-        nd = 4;
-        ext[0] = s.T; ext[1] = 3; ext[2] = s.H; ext[3] = s.D;
-    } else {
-        nd = 3;
-        ext[0] = s.T; ext[1] = s.H; ext[2] = s.D;
+    // Geometry of one strided slab view [T][heads_view][D].
+    const int64_t ext[3] = {s.T, rq.heads_view, s.D};
+    for (int i = 0; i < 3; ++i) {
+        if (rq.str[i] < 0) return VF_ERR_ARG;
+        if (ext[i] <= 1) rq.str[i] = 0;          // unused: the index is always 0
     }
-    if (strides) {
-        for (int i = 0; i < nd; ++i) str[i] = strides[i];
-    } else if (s.op == VF_OP_HEAD_MERGE) {
-        str[0] = s.H * s.D; str[1] = s.D; str[2] = 1;
-    } else {
-        return VF_ERR_ARG;
-    }
-    for (int i = 0; i < nd; ++i) {
-        if (str[i] < 0) return VF_ERR_ARG;
-        if (ext[i] <= 1) str[i] = 0;             // unused: the index is always 0
-    }
-    int64_t span;
-    if ((rc = max_offset(ext, str, nd, &span)) != VF_OK) return rc;
-    int64_t strided_bytes;
-    if (!add_ok(span, 1, &strided_bytes) || !mul_ok(strided_bytes, 2, &strided_bytes))
+    int64_t span, view_bytes;
+    if ((rc = max_offset(ext, rq.str, 3, &span)) != VF_OK) return rc;
+    if (!add_ok(span, 1, &view_bytes) || !mul_ok(view_bytes, 2, &view_bytes))
         return VF_ERR_OVERFLOW;
 
     const int64_t n = packed_elems(s);
-    if (n == 0) return VF_OK;
-    if (src == nullptr || dst == nullptr) return VF_ERR_ARG;
-    // 16-bit elements: both pointers must be 2-byte aligned
-    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 1u)
-        return VF_ERR_ARG;
-    if (s.op == VF_OP_HEAD_MERGE && !non_overlapping(ext, str, nd)) return VF_ERR_ARG;
+    if (n == 0 || rq.c_begin == rq.c_end) return VF_OK;
 
-    const bool packed_is_dst = s.op != VF_OP_HEAD_MERGE;
-    const void *packed = packed_is_dst ? static_cast<const void *>(dst) : src;
-    const void *strided = packed_is_dst ? src : static_cast<const void *>(dst);
-    const uintptr_t pa = reinterpret_cast<uintptr_t>(packed);
-    const uintptr_t sa = reinterpret_cast<uintptr_t>(strided);
-    if (pa > UINTPTR_MAX - uint64_t(2 * n) || sa > UINTPTR_MAX - uint64_t(strided_bytes))
-        return VF_ERR_OVERFLOW;
-    if (ranges_overlap(pa, uint64_t(2 * n), sa, uint64_t(strided_bytes))) return VF_ERR_ALIAS;
+    // Pointers: present, 2-byte aligned, ranges inside the address space.
+    if (rq.packed == nullptr) return VF_ERR_ARG;
+    uintptr_t bits = reinterpret_cast<uintptr_t>(rq.packed);
+    for (int64_t i = 0; i < slabs; ++i) {
+        if (rq.strided[i] == nullptr) return VF_ERR_ARG;
+        bits |= reinterpret_cast<uintptr_t>(rq.strided[i]);
+    }
+    if (bits & 1u) return VF_ERR_ARG;
+    if (rq.strided_written && !non_overlapping(ext, rq.str, 3)) return VF_ERR_ARG;
 
-    if ((rc = check_pointer(src)) != VF_OK) return rc;
-    if ((rc = check_pointer(dst)) != VF_OK) return rc;
+    const Range packed{reinterpret_cast<uintptr_t>(rq.packed), uint64_t(2 * n)};
+    if (packed.lo > UINTPTR_MAX - packed.len) return VF_ERR_OVERFLOW;
+    Range views[3];
+    for (int64_t i = 0; i < slabs; ++i) {
+        views[i] = {reinterpret_cast<uintptr_t>(rq.strided[i]), uint64_t(view_bytes)};
+        if (views[i].lo > UINTPTR_MAX - views[i].len) return VF_ERR_OVERFLOW;
+        if (overlap(packed, views[i])) return VF_ERR_ALIAS;
+    }
+    if (rq.strided_written)
+        for (int64_t i = 0; i < slabs; ++i)
+            for (int64_t j = i + 1; j < slabs; ++j)
+                if (overlap(views[i], views[j])) return VF_ERR_ALIAS;
+
+    if ((rc = check_pointer(rq.packed)) != VF_OK) return rc;
+    for (int64_t i = 0; i < slabs; ++i) {
+        bool seen = false;
+        for (int64_t j = 0; j < i; ++j) seen = seen || rq.strided[j] == rq.strided[i];
+        if (!seen && (rc = check_pointer(rq.strided[i])) != VF_OK) return rc;
+    }
 
     Plan pl;
-    pl.src = static_cast<const uint16_t *>(src);
-    pl.dst = static_cast<uint16_t *>(dst);
-    pl.packed_is_dst = packed_is_dst;
+    pl.packed = static_cast<uint16_t *>(rq.packed);
+    pl.row_stride = rq.str[0];
+    pl.head_stride = rq.str[1];
+    pl.d_stride = rq.str[2];
+    pl.heads = heads_per_row(s);
     pl.D = s.D;
-    const std::vector<Entry> table = piece_table(s);
-    pl.pieces.reserve(table.size());
-    if (s.op == VF_OP_QKV_PACK) {
-        const int64_t Hp = s.H / s.P;
-        pl.row_stride = str[0];
-        pl.slab_stride = str[1];
-        pl.head_stride = str[2];
-        pl.d_stride = str[3];
-        pl.heads = Hp;
-        pl.slabs = 3;
-        for (size_t e = 0; e < table.size(); ++e) {
-            const int64_t p = int64_t(e) % s.P;
-            pl.pieces.push_back({table[e].packed_off,
-                                 table[e].tok_start * str[0] + p * Hp * str[2],
-                                 table[e].tok_len});
-        }
-    } else if (s.op == VF_OP_ATTN_SPLIT) {
-        pl.row_stride = str[0];
-        pl.head_stride = str[1];
-        pl.d_stride = str[2];
-        pl.slab_stride = 0;
-        pl.heads = s.H;
-        pl.slabs = 1;
-        for (const Entry &e : table)
-            pl.pieces.push_back({e.packed_off, e.tok_start * str[0], e.tok_len});
-    } else {
-        const int64_t Hp = s.H / s.P;
-        pl.row_stride = str[0];
-        pl.head_stride = str[1];
-        pl.d_stride = str[2];
-        pl.slab_stride = 0;
-        pl.heads = Hp;
-        pl.slabs = 1;
-        for (size_t e = 0; e < table.size(); ++e) {
-            const int64_t p = int64_t(e) % s.P;
-            pl.pieces.push_back({table[e].packed_off,
-                                 table[e].tok_start * str[0] + p * Hp * str[1],
-                                 table[e].tok_len});
-        }
-    }
     if (pl.heads > INT32_MAX || pl.D > INT32_MAX) return VF_ERR_ARG;
 
-    const int vw = pick_vector_width(pl, packed, strided);
+    // Pieces of the requested chunks, one per (c, p, slab).  Pack and merge
+    // address head group p of a full-head view; the split and the unpack
+    // address all heads of their view.  A pack or unpack block holds its
+    // q, k, v slabs back to back, each rows x heads x D.
+    const std::vector<Entry> table = piece_table(s);
+    const int64_t group_heads = (s.op == VF_OP_QKV_PACK || s.op == VF_OP_HEAD_MERGE)
+                                    ? s.H / s.P : 0;
+    const int64_t R = pl.heads * pl.D;
+    for (int64_t c = rq.c_begin; c < rq.c_end; ++c)
+        for (int64_t p = 0; p < s.P; ++p) {
+            const Entry &e = table[size_t(c * s.P + p)];
+            // element offset of the block's first row in each slab view; it
+            // lies inside the view (checked extent), so it cannot overflow
+            const int64_t off = e.tok_start * rq.str[0] + p * group_heads * rq.str[1];
+            for (int64_t sl = 0; sl < slabs; ++sl) {
+                uint16_t *base = const_cast<uint16_t *>(
+                    static_cast<const uint16_t *>(rq.strided[sl]));
+                pl.pieces.push_back({e.packed_off + sl * e.tok_len * R, base + off, e.tok_len});
+            }
+        }
+
+    const int vw = pick_vector_width(pl);
+    const bool packed_is_dst = s.op == VF_OP_QKV_PACK || s.op == VF_OP_ATTN_SPLIT;
     return packed_is_dst ? launch_dir<true>(pl, vw, stream) : launch_dir<false>(pl, vw, stream);
+}
+
+cudaStream_t as_stream(vf_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Chunk range [c_begin, c_begin + c_count) without overflow; run() checks it.
+int64_t range_end(int64_t c_begin, int64_t c_count) {
+    int64_t e;
+    if (c_count < 0 || !add_ok(c_begin, c_count, &e)) return -1;
+    return e;
+}
+
+int pack_common(const void *q, const void *k, const void *v, const int64_t *str,
+                int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, int64_t c_begin,
+                int64_t c_count, void *dst, vf_stream_t stream) {
+    Request rq{};
+    rq.s = {VF_OP_QKV_PACK, T, H, D, P, C};
+    rq.c_begin = c_begin;
+    rq.c_end = range_end(c_begin, c_count);
+    rq.packed = dst;
+    rq.strided[0] = q;
+    rq.strided[1] = k;
+    rq.strided[2] = v;
+    for (int i = 0; i < 3; ++i) rq.str[i] = str[i];
+    rq.heads_view = H;
+    rq.strided_written = false;
+    return run(rq, as_stream(stream));
+}
+
+int pack4(const void *src, const int64_t src_strides[4], int64_t T, int64_t H, int64_t D,
+          int64_t P, int64_t C, int64_t c_begin, int64_t c_count, void *dst,
+          vf_stream_t stream) {
+    if (src_strides == nullptr) return VF_ERR_ARG;
+    const int64_t ss = src_strides[1];
+    if (ss < 0) return VF_ERR_ARG;
+    const int64_t str[3] = {src_strides[0], src_strides[2], src_strides[3]};
+    if (src == nullptr)      // only legal when nothing is moved; run() decides
+        return pack_common(nullptr, nullptr, nullptr, str, T, H, D, P, C, c_begin, c_count,
+                           dst, stream);
+    // slab s of the [T][3][H][D] view starts s * ss elements after src
+    int64_t off2;
+    if (!mul_ok(ss, 4, &off2)) return VF_ERR_OVERFLOW;                 // 2 slabs x 2 bytes
+    const uintptr_t base = reinterpret_cast<uintptr_t>(src);
+    if (base > UINTPTR_MAX - uint64_t(off2)) return VF_ERR_OVERFLOW;
+    const char *b = static_cast<const char *>(src);
+    return pack_common(src, b + 2 * ss, b + 4 * ss, str, T, H, D, P, C, c_begin, c_count, dst,
+                       stream);
+}
+
+int split_common(const void *src, const int64_t src_strides[3], int64_t T, int64_t H,
+                 int64_t D, int64_t P, int64_t C, int64_t c_begin, int64_t c_count, void *dst,
+                 vf_stream_t stream) {
+    if (src_strides == nullptr) return VF_ERR_ARG;
+    Request rq{};
+    rq.s = {VF_OP_ATTN_SPLIT, T, H, D, P, C};
+    rq.c_begin = c_begin;
+    rq.c_end = range_end(c_begin, c_count);
+    rq.packed = dst;
+    rq.strided[0] = src;
+    for (int i = 0; i < 3; ++i) rq.str[i] = src_strides[i];
+    rq.heads_view = H;
+    rq.strided_written = false;
+    return run(rq, as_stream(stream));
+}
+
+int merge_common(const void *src, const int64_t dst_strides[3], int64_t T, int64_t H,
+                 int64_t D, int64_t P, int64_t C, int64_t c_begin, int64_t c_count, void *dst,
+                 vf_stream_t stream) {
+    Request rq{};
+    rq.s = {VF_OP_HEAD_MERGE, T, H, D, P, C};
+    rq.c_begin = c_begin;
+    rq.c_end = range_end(c_begin, c_count);
+    rq.packed = const_cast<void *>(src);
+    rq.strided[0] = dst;
+    if (dst_strides) {
+        for (int i = 0; i < 3; ++i) rq.str[i] = dst_strides[i];
+    } else {
+        if (H < 0 || D < 0 || !mul_ok(H, D, &rq.str[0])) return VF_ERR_ARG;
+        rq.str[1] = D;
+        rq.str[2] = 1;
+    }
+    rq.heads_view = H;
+    rq.strided_written = true;
+    return run(rq, as_stream(stream));
+}
+
+int unpack_common(const void *recv, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                  int64_t c_begin, int64_t c_count, void *q, void *k, void *v,
+                  const int64_t out_strides[3], vf_stream_t stream) {
+    if (P < 1 || H < 0 || D < 0 || H % P != 0) return VF_ERR_ARG;
+    Request rq{};
+    rq.s = {VF_OP_QKV_UNPACK, T, H, D, P, C};
+    rq.c_begin = c_begin;
+    rq.c_end = range_end(c_begin, c_count);
+    rq.packed = const_cast<void *>(recv);
+    rq.strided[0] = q;
+    rq.strided[1] = k;
+    rq.strided[2] = v;
+    const int64_t Hp = H / P;
+    if (out_strides) {
+        for (int i = 0; i < 3; ++i) rq.str[i] = out_strides[i];
+    } else {
+        if (!mul_ok(Hp, D, &rq.str[0])) return VF_ERR_OVERFLOW;
+        rq.str[1] = D;
+        rq.str[2] = 1;
+    }
+    rq.heads_view = Hp;
+    rq.strided_written = true;
+    return run(rq, as_stream(stream));
 }
 
 }  // namespace
@@ -354,20 +472,54 @@ extern "C" {
 
 int vf_qkv_pack(const void *src, const int64_t src_strides[4], int64_t T, int64_t H,
                 int64_t D, int64_t P, int64_t C, void *dst, vf_stream_t stream) {
-    return run({VF_OP_QKV_PACK, T, H, D, P, C}, src, src_strides, dst,
-               reinterpret_cast<cudaStream_t>(stream));
+    return pack4(src, src_strides, T, H, D, P, C, 0, C, dst, stream);
+}
+
+int vf_qkv_pack_chunks(const void *src, const int64_t src_strides[4], int64_t T, int64_t H,
+                       int64_t D, int64_t P, int64_t C, int64_t c_begin, int64_t c_count,
+                       void *dst, vf_stream_t stream) {
+    return pack4(src, src_strides, T, H, D, P, C, c_begin, c_count, dst, stream);
+}
+
+int vf_qkv_pack3(const void *q, const void *k, const void *v, const int64_t qkv_strides[3],
+                 int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, int64_t c_begin,
+                 int64_t c_count, void *dst, vf_stream_t stream) {
+    if (qkv_strides == nullptr) return VF_ERR_ARG;
+    return pack_common(q, k, v, qkv_strides, T, H, D, P, C, c_begin, c_count, dst, stream);
 }
 
 int vf_attn_split(const void *src, const int64_t src_strides[3], int64_t T, int64_t H,
                   int64_t D, int64_t P, int64_t C, void *dst, vf_stream_t stream) {
-    return run({VF_OP_ATTN_SPLIT, T, H, D, P, C}, src, src_strides, dst,
-               reinterpret_cast<cudaStream_t>(stream));
+    return split_common(src, src_strides, T, H, D, P, C, 0, C, dst, stream);
+}
+
+int vf_attn_split_chunks(const void *src, const int64_t src_strides[3], int64_t T,
+                         int64_t H, int64_t D, int64_t P, int64_t C, int64_t c_begin,
+                         int64_t c_count, void *dst, vf_stream_t stream) {
+    return split_common(src, src_strides, T, H, D, P, C, c_begin, c_count, dst, stream);
 }
 
 int vf_head_merge(const void *src, const int64_t dst_strides[3], int64_t T, int64_t H,
                   int64_t D, int64_t P, int64_t C, void *dst, vf_stream_t stream) {
-    return run({VF_OP_HEAD_MERGE, T, H, D, P, C}, src, dst_strides, dst,
-               reinterpret_cast<cudaStream_t>(stream));
+    return merge_common(src, dst_strides, T, H, D, P, C, 0, C, dst, stream);
+}
+
+int vf_head_merge_chunks(const void *src, const int64_t dst_strides[3], int64_t T,
+                         int64_t H, int64_t D, int64_t P, int64_t C, int64_t c_begin,
+                         int64_t c_count, void *dst, vf_stream_t stream) {
+    return merge_common(src, dst_strides, T, H, D, P, C, c_begin, c_count, dst, stream);
+}
+
+int vf_qkv_unpack(const void *recv, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                  void *q, void *k, void *v, const int64_t out_strides[3],
+                  vf_stream_t stream) {
+    return unpack_common(recv, T, H, D, P, C, 0, C, q, k, v, out_strides, stream);
+}
+
+int vf_qkv_unpack_chunks(const void *recv, int64_t T, int64_t H, int64_t D, int64_t P,
+                         int64_t C, int64_t c_begin, int64_t c_count, void *q, void *k,
+                         void *v, const int64_t out_strides[3], vf_stream_t stream) {
+    return unpack_common(recv, T, H, D, P, C, c_begin, c_count, q, k, v, out_strides, stream);
 }
 
 int64_t vf_packed_elems(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C) {

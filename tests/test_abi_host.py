@@ -41,7 +41,9 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     for want in ("vf_qkv_pack", "vf_attn_split", "vf_head_merge", "vf_packed_elems",
-                 "vf_piece_table", "vf_status_string"):
+                 "vf_piece_table", "vf_status_string", "vf_qkv_unpack", "vf_qkv_pack3",
+                 "vf_qkv_pack_chunks", "vf_attn_split_chunks", "vf_head_merge_chunks",
+                 "vf_qkv_unpack_chunks"):
         assert want in names
 
 
@@ -90,7 +92,9 @@ def test_piece_tables_match_hand_derivation(L):
                                    (37, 6, 16, 3, 7), (4, 6, 2, 6, 16)])
 def test_piece_tables_match_oracle(L, shape):
     T, H, D, P, C = shape
-    for op in (0, 1, 2):
+    for op in (0, 1, 2, 3):
+        if op != 1 and H % P:
+            continue
         assert vf.piece_table(op, T, H, D, P, C) == loops.piece_table(op, T, H, D, P, C)
 
 
@@ -136,6 +140,44 @@ def test_empty_calls_return_ok_without_cuda(L, fn, strides):
     # T = 0, H = 0 or D = 0: nothing to move, no pointer is needed
     for T, H, D in ((0, 4, 8), (4, 0, 8), (4, 4, 0)):
         assert _call(L, fn, None, strides, T, H, D, 2, 3, None) == 0
+
+
+def _i64(*xs):
+    return (I64 * len(xs))(*xs)
+
+
+def test_unpack_and_range_rejections(L):
+    Q, K, V = FAKE_DST, FAKE_DST + (1 << 20), FAKE_DST + (2 << 20)
+    st = _i64(16, 8, 1)
+    # H % P, aliasing outputs, output overlapping the received buffer
+    assert L.vf_qkv_unpack(FAKE_SRC, 4, 6, 8, 4, 2, Q, K, V, st, None) == -1
+    assert L.vf_qkv_unpack(FAKE_SRC, 4, 4, 8, 2, 2, Q, Q, V, st, None) == -3
+    assert L.vf_qkv_unpack(FAKE_SRC, 4, 4, 8, 2, 2, Q, K, FAKE_SRC + 8, st, None) == -3
+    assert L.vf_qkv_unpack(FAKE_SRC, 4, 4, 8, 2, 2, Q, K, V, _i64(0, 8, 1), None) == -1
+    assert L.vf_qkv_unpack(FAKE_SRC, 4, 4, 8, 2, 2, Q + 1, K, V, st, None) == -1
+    # chunk ranges
+    s4 = _i64(96, 32, 8, 1)
+    for c0, cn in ((-1, 1), (0, -1), (2, 1), (1, 2), (3, 0)):
+        assert L.vf_qkv_pack_chunks(FAKE_SRC, s4, 4, 4, 8, 2, 2, c0, cn, FAKE_DST, None) == -1
+        assert L.vf_attn_split_chunks(FAKE_SRC, _i64(32, 8, 1), 4, 4, 8, 2, 2, c0, cn,
+                                      FAKE_DST, None) == -1
+        assert L.vf_head_merge_chunks(FAKE_SRC, None, 4, 4, 8, 2, 2, c0, cn, FAKE_DST,
+                                      None) == -1
+        assert L.vf_qkv_unpack_chunks(FAKE_SRC, 4, 4, 8, 2, 2, c0, cn, Q, K, V, st, None) == -1
+    # an empty chunk range moves nothing and needs no GPU
+    assert L.vf_qkv_pack_chunks(FAKE_SRC, s4, 4, 4, 8, 2, 2, 1, 0, FAKE_DST, None) == 0
+    assert L.vf_qkv_unpack_chunks(FAKE_SRC, 4, 4, 8, 2, 2, 2, 0, Q, K, V, st, None) == 0
+    # three-pointer pack: strides required; q, k, v may overlap (read only) but
+    # not the destination
+    assert L.vf_qkv_pack3(FAKE_SRC, FAKE_SRC, FAKE_SRC, None, 4, 4, 8, 2, 2, 0, 2,
+                          FAKE_DST, None) == -1
+    assert L.vf_qkv_pack3(FAKE_SRC, FAKE_SRC, FAKE_DST, _i64(32, 8, 1), 4, 4, 8, 2, 2, 0, 2,
+                          FAKE_DST + 16, None) == -3
+
+
+def test_packed_elems_unpack(L):
+    assert vf.packed_elems(vf.OP_QKV_UNPACK, 55414, 28, 128, 2, 4) == 3 * 55414 * 14 * 128
+    assert L.vf_packed_elems(3, 10, 3, 8, 2, 2) == -1
 
 
 def test_piece_table_capacity(L):
