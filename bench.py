@@ -391,6 +391,8 @@ def gpu_arm(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         e2e = e2e_arm(args, cfg, dev, world)
 
+    configs = per_config(args, dev) if args.configs else None
+
     line = None
     if rank == 0:
         line = {
@@ -413,55 +415,209 @@ def gpu_arm(args, rank, world, local_rank):
             "clocks": clock_info,
             "gpu_launches": K * launches_per_step(cfg, len(ops_run)),
             "e2e": e2e,
+            "per_config": configs,
         }
     return line
 
 
 def e2e_arm(args, cfg, dev, world):
-    """Same metric through the public API from pinned host buffers: every
-    step copies its inputs host->device, runs the three relayouts and copies
-    the outputs device->host."""
+    """Same metric through the public API from pinned host buffers.
+
+    Every step copies its inputs host->device, runs the three relayouts and
+    copies the outputs device->host.  The step is pipelined over the C overlap
+    chunks on three streams (copy in, relayout, copy out) with the chunk-range
+    entry points, so the two copy directions and the kernels overlap; events
+    order chunk c of step i+1 after chunk c of step i.  A serial variant (one
+    stream, whole tensors) is reported beside it."""
+    import torch
+
+    import sequence_head_relayout_gb300 as vf
+
+    T, H, D, P, C = cfg.T, cfg.H, cfg.D, cfg.P, cfg.C
+    d = make_set(cfg, dev, 33)
+    keys_in = ("pack_base", "split_base", "merge_src")
+    keys_out = ("pack_dst", "split_dst", "merge_dst")
+    host = {k: torch.empty(d[k].shape, dtype=torch.int16, pin_memory=True)
+            for k in keys_in + keys_out}
+    for k in keys_in:
+        host[k].copy_(d[k])
+    torch.cuda.synchronize()
+    h2d = sum(host[k].numel() * 2 for k in keys_in)
+    d2h = sum(host[k].numel() * 2 for k in keys_out)
+
+    def token_major(dv, hv):
+        """Buffers whose outermost axis is the token: rows [t0, t1)."""
+        a, b = dv.view(T, -1), hv.view(T, -1)
+        return lambda t0, t1: [(a[t0:t1], b[t0:t1])]
+
+    def head_major(dv, hv):
+        """[X, T, D] buffers: rows [t0, t1) of every head plane."""
+        a, b = dv.view(-1, T, D), hv.view(-1, T, D)
+        return lambda t0, t1: [(a[x, t0:t1], b[x, t0:t1]) for x in range(a.shape[0])]
+
+    pack_in = token_major(d["pack_base"], host["pack_base"])
+    split_in = (head_major if cfg.split_src == "bhtd" else token_major)(d["split_base"],
+                                                                         host["split_base"])
+    merge_out = token_major(d["merge_dst"], host["merge_dst"])    # make_set: contiguous
+    pk = vf.piece_table(vf.OP_QKV_PACK, T, H, D, P, C)
+    sp = vf.piece_table(vf.OP_ATTN_SPLIT, T, H, D, P, C)
+    mg = vf.piece_table(vf.OP_HEAD_MERGE, T, H, D, P, C)
+
+    def slab(table, c, total):
+        a = table[2][c * P]
+        b = table[2][(c + 1) * P] if c + 1 < C else total
+        return a, b
+
+    n_pack, n_split = d["pack_dst"].numel(), d["split_dst"].numel()
+    n_merge = d["merge_src"].numel()
+    s_in, s_k, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    done_k = [None] * C       # relayout of chunk c finished (inputs free)
+    done_out = [None] * C     # copy-out of chunk c finished (outputs free)
+
+    def pipelined_step():
+        for c in range(C):
+            t0 = mg[0][c * P]
+            t1 = t0 + mg[1][c * P]
+            with torch.cuda.stream(s_in):
+                if done_k[c] is not None:
+                    s_in.wait_event(done_k[c])
+                for dv, hv in pack_in(t0, t1):
+                    dv.copy_(hv, non_blocking=True)
+                for p in range(P):
+                    e = c * P + p
+                    for dv, hv in split_in(sp[0][e], sp[0][e] + sp[1][e]):
+                        dv.copy_(hv, non_blocking=True)
+                a, b = slab(mg, c, n_merge)
+                d["merge_src"][a:b].copy_(host["merge_src"][a:b], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            s_k.wait_event(ready)
+            if done_out[c] is not None:
+                s_k.wait_event(done_out[c])
+            vf.qkv_pack(d["pack_src"], P, C, out=d["pack_dst"], stream=s_k, chunks=(c, 1))
+            vf.attn_split(d["split_src"], P, C, out=d["split_dst"], stream=s_k, chunks=(c, 1))
+            vf.head_merge(d["merge_src"], T, H, D, P, C, out=d["merge_dst"], stream=s_k,
+                          chunks=(c, 1))
+            done_k[c] = torch.cuda.Event()
+            done_k[c].record(s_k)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_k[c])
+                a, b = slab(pk, c, n_pack)
+                host["pack_dst"][a:b].copy_(d["pack_dst"][a:b], non_blocking=True)
+                a, b = slab(sp, c, n_split)
+                host["split_dst"][a:b].copy_(d["split_dst"][a:b], non_blocking=True)
+                for dv, hv in merge_out(t0, t1):
+                    hv.copy_(dv, non_blocking=True)
+                done_out[c] = torch.cuda.Event()
+                done_out[c].record(s_out)
+
+    def serial_step():
+        for k in keys_in:
+            d[k].copy_(host[k], non_blocking=True)
+        run_step(vf, cfg, d)
+        for k in keys_out:
+            host[k].copy_(d[k], non_blocking=True)
+
+    step_bytes = sum(alg_bytes(x) for x in op_elements(cfg).values())
+    n = max(3, min(args.steps, 20))
+
+    def timed(step, streams):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(streams[0])
+        for st in streams[1:]:
+            st.wait_event(a)
+        for _ in range(n):
+            step()
+        for st in streams[:-1]:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            streams[-1].wait_event(ev)
+        b.record(streams[-1])
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    ms = timed(pipelined_step, [s_in, s_k, s_out])
+    # the last copied-out outputs must be the relayouts of the copied-in inputs
+    ok = (torch.equal(host["pack_dst"], d["pack_dst"].cpu())
+          and torch.equal(host["split_dst"], d["split_dst"].cpu())
+          and torch.equal(host["merge_dst"], d["merge_dst"].cpu()))
+    cur = torch.cuda.current_stream(dev)
+    serial_ms = timed(serial_step, [cur])
+    return {"value": round(world * n * step_bytes / (ms / 1e3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": round(ms / n, 3),
+            "mode": "pipelined over %d chunks on 3 streams (copy in, relayout, copy out)" % C,
+            "outputs_checked": bool(ok),
+            "serial": {"value": round(world * n * step_bytes / (serial_ms / 1e3) / 1e9, 1),
+                       "ms_per_step": round(serial_ms / n, 3)}}
+
+
+def per_config(args, dev):
+    """Median time and effective GB/s of every relayout at every workload.
+
+    The small workloads fit in L2, so every rep is preceded by a write of a
+    256 MB buffer (twice the 129 MB L2) outside the timed region; the events
+    bracket the relayout alone, on its launching stream."""
     import torch
 
     import sequence_head_relayout_gb300 as vf
     from sequence_head_relayout_gb300 import workloads as W
 
-    d = make_set(cfg, dev, 33)
-    host = {k: torch.empty(d[k].shape, dtype=torch.int16, pin_memory=True)
-            for k in ("pack_base", "split_base", "merge_src", "pack_dst", "split_dst",
-                      "merge_dst")}
-    host["pack_base"].copy_(d["pack_base"])
-    host["split_base"].copy_(d["split_base"])
-    host["merge_src"].copy_(d["merge_src"])
-    torch.cuda.synchronize()
-    h2d = sum(host[k].numel() * 2 for k in ("pack_base", "split_base", "merge_src"))
-    d2h = sum(host[k].numel() * 2 for k in ("pack_dst", "split_dst", "merge_dst"))
-
-    def step():
-        d["pack_base"].copy_(host["pack_base"], non_blocking=True)
-        d["split_base"].copy_(host["split_base"], non_blocking=True)
-        d["merge_src"].copy_(host["merge_src"], non_blocking=True)
-        run_step(vf, cfg, d)
-        host["pack_dst"].copy_(d["pack_dst"], non_blocking=True)
-        host["split_dst"].copy_(d["split_dst"], non_blocking=True)
-        host["merge_dst"].copy_(d["merge_dst"], non_blocking=True)
-
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize()
-    n = max(3, min(args.steps, 20))
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    step_bytes = sum(alg_bytes(x) for x in op_elements(cfg).values())
-    return {"value": round(world * n * step_bytes / (ms / 1e3) / 1e9, 1), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "ms_per_step": round(ms / n, 3)}
+    peak, _ = measured_peak()
+    flush = torch.empty(128 << 20, dtype=torch.int16, device=dev)
+    reps = max(5, args.config_reps)
+    table = {}
+    for name in args.configs:
+        cfg = W.CONFIGS[name]
+        T, H, D, P, C = cfg.T, cfg.H, cfg.D, cfg.P, cfg.C
+        Hp = H // P
+        pack_src, _ = W.pack_source(cfg, device=dev)
+        split_src, _ = W.split_source(cfg, device=dev)
+        merge_src = W.merge_source(cfg, device=dev)
+        merge_dst, _ = W.merge_destination(cfg, device=dev)
+        recv = torch.empty(3 * T * Hp * D, dtype=torch.int16, device=dev)
+        W.fill_(recv, cfg.payload, cfg.seed + 3000)
+        outs = tuple(torch.empty((T, Hp, D), dtype=torch.int16, device=dev) for _ in range(3))
+        pack_dst = torch.empty(3 * T * H * D, dtype=torch.int16, device=dev)
+        split_dst = torch.empty(T * H * D, dtype=torch.int16, device=dev)
+        ops = {
+            "qkv_pack": (3 * T * H * D,
+                         lambda: vf.qkv_pack(pack_src, P, C, out=pack_dst)),
+            "attn_split": (T * H * D, lambda: vf.attn_split(split_src, P, C, out=split_dst)),
+            "head_merge": (T * H * D, lambda: vf.head_merge(merge_src, T, H, D, P, C,
+                                                             out=merge_dst)),
+            "qkv_unpack": (3 * T * Hp * D, lambda: vf.qkv_unpack(recv, T, H, D, P, C,
+                                                                 outs=outs)),
+            "qkv_pack3": (3 * T * H * D, lambda: vf.qkv_pack3(
+                pack_src[:, 0], pack_src[:, 1], pack_src[:, 2], P, C, out=pack_dst)),
+        }
+        row = {}
+        for op, (elems, fn) in ops.items():
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(reps):
+                flush.fill_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            med = statistics.median(x.elapsed_time(y) for x, y in ts)
+            gbs = alg_bytes(elems) / (med / 1e3) / 1e9
+            row[op] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
+                       "frac_of_peak": round(gbs / peak, 4)}
+        table[name] = row
+        del pack_src, split_src, merge_src, merge_dst, recv, outs, pack_dst, split_dst
+        torch.cuda.empty_cache()
+    return {"reps": reps, "l2": "256 MB buffer written between reps, outside the events",
+            "table": table}
 
 
 # ----------------------------------------------------------------------------
@@ -519,6 +675,9 @@ def main():
     ap.add_argument("--only", nargs="+", choices=["qkv_pack", "attn_split", "head_merge"],
                     help="time only these relayouts (profiling runs)")
     ap.add_argument("--sets", type=int, default=2, help="rotating input/output buffer sets")
+    ap.add_argument("--configs", nargs="*", default=["tiny", "4k", "pages", "ragged", "large"],
+                    help="workloads for the per-op, per-workload table (none to skip)")
+    ap.add_argument("--config-reps", type=int, default=30)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
