@@ -540,20 +540,48 @@ def e2e_arm(args, cfg, dev, world):
         torch.cuda.synchronize()
         return a.elapsed_time(b)
 
-    ms = timed(pipelined_step, [s_in, s_k, s_out])
-    # the last copied-out outputs must be the relayouts of the copied-in inputs
-    ok = (torch.equal(host["pack_dst"], d["pack_dst"].cpu())
-          and torch.equal(host["split_dst"], d["split_dst"].cpu())
-          and torch.equal(host["merge_dst"], d["merge_dst"].cpu()))
+    # zero copy: the kernels read the pinned host inputs and write the pinned
+    # host outputs directly over the host link, one pass, no staging copies
+    def host_view(dev_view, base):
+        return torch.as_strided(host[base], dev_view.size(), dev_view.stride(),
+                                dev_view.storage_offset())
+
+    hz_pack = host_view(d["pack_src"], "pack_base")
+    hz_split = host_view(d["split_src"], "split_base")
+
+    def zero_copy_step():
+        vf.qkv_pack(hz_pack, P, C, out=host["pack_dst"])
+        vf.attn_split(hz_split, P, C, out=host["split_dst"])
+        vf.head_merge(host["merge_src"], T, H, D, P, C, out=host["merge_dst"])
+
+    def outputs_match():
+        return bool(torch.equal(host["pack_dst"], d["pack_dst"].cpu())
+                    and torch.equal(host["split_dst"], d["split_dst"].cpu())
+                    and torch.equal(host["merge_dst"], d["merge_dst"].cpu()))
+
     cur = torch.cuda.current_stream(dev)
-    serial_ms = timed(serial_step, [cur])
-    return {"value": round(world * n * step_bytes / (ms / 1e3) / 1e9, 1), "unit": UNIT,
+    modes = {}
+    for name, fn, streams in (
+            ("pipelined", pipelined_step, [s_in, s_k, s_out]),
+            ("zero_copy", zero_copy_step, [cur]),
+            ("serial", serial_step, [cur])):
+        for k in keys_out:
+            host[k].fill_(0)
+        ms = timed(fn, streams)
+        # the last outputs on the host must be the relayouts of the inputs
+        modes[name] = {"value": round(world * n * step_bytes / (ms / 1e3) / 1e9, 1),
+                       "ms_per_step": round(ms / n, 3), "outputs_checked": outputs_match()}
+    desc = {"pipelined": "copies pipelined over the %d overlap chunks on 3 streams "
+                         "(copy in, chunk-range relayouts, copy out)" % C,
+            "zero_copy": "kernels read pinned host inputs and write pinned host outputs "
+                         "directly over the host link",
+            "serial": "whole-tensor copy in, relayouts, copy out on one stream"}
+    best = max((m for m in modes if modes[m]["outputs_checked"]),
+               key=lambda m: modes[m]["value"])
+    return {"value": modes[best]["value"], "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "ms_per_step": round(ms / n, 3),
-            "mode": "pipelined over %d chunks on 3 streams (copy in, relayout, copy out)" % C,
-            "outputs_checked": bool(ok),
-            "serial": {"value": round(world * n * step_bytes / (serial_ms / 1e3) / 1e9, 1),
-                       "ms_per_step": round(serial_ms / n, 3)}}
+            "ms_per_step": modes[best]["ms_per_step"], "mode": best,
+            "mode_description": desc[best], "modes": modes}
 
 
 def per_config(args, dev):

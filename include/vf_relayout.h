@@ -32,8 +32,10 @@
  * allocates no memory, keeps no global state, never synchronises, and is
  * safe to call from several host threads.  Work is enqueued on `stream`
  * (NULL = the legacy default stream) of the current device; every pointer
- * must be accessible from that device (device, managed or mapped pinned
- * memory).  The call returns once the kernels are enqueued.
+ * must be accessible from that device: device memory of that device, managed
+ * memory, or page-locked host memory mapped at the same address (the kernels
+ * then read or write it directly over the host link).  The call returns once
+ * the kernels are enqueued.
  *
  * Errors: every function returns VF_OK (0) or a negative vf_status.  All
  * argument checks run on the host before anything is enqueued, so a

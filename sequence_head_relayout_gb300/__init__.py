@@ -5,7 +5,9 @@ Thin ctypes binding over ``libvf_relayout.so`` (C ABI in
 strides and the current CUDA stream; every element is moved by the library's
 sm_103a kernels.  PyTorch provides device memory and streams.  There is no
 CPU path: the library must be built (``__graft_entry__.build()``) and the
-tensors must live on a CUDA device, otherwise the calls raise.
+tensors must be addressable by the GPU -- CUDA memory, or pinned host memory
+that the kernels read or write directly over the host link -- otherwise the
+calls raise.
 
 Operations ("Sol-Engine alignment on SM86 and SM89", section "What is
 enabled"):
@@ -84,10 +86,14 @@ def lib():
 
 
 def _check16(t: torch.Tensor, what: str):
+    """A 16-bit tensor the GPU can address: CUDA memory, or pinned (page-locked,
+    mapped) host memory, which the kernels read and write directly over the
+    host link.  Pageable host memory is refused: there is no CPU path."""
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % what)
-    if t.device.type != "cuda":
-        raise ValueError("%s must be a CUDA tensor (there is no CPU path)" % what)
+    if t.device.type != "cuda" and not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError("%s must be a CUDA tensor or pinned host memory "
+                         "(there is no CPU path)" % what)
     if t.element_size() != 2:
         raise ValueError("%s must hold 16-bit elements (bf16/fp16/int16)" % what)
 
@@ -97,8 +103,10 @@ def _strides(t: torch.Tensor):
 
 
 def _stream(stream, device):
+    """The stream to enqueue on: the given one, else the current stream of the
+    tensor's device (of the current device for pinned host tensors)."""
     if stream is None:
-        stream = torch.cuda.current_stream(device)
+        stream = torch.cuda.current_stream(device if device.type == "cuda" else None)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -132,7 +140,8 @@ def _range(chunks, C):
 
 def _flat_out(out, n, like):
     if out is None:
-        out = torch.empty(n, dtype=like.dtype, device=like.device)
+        out = torch.empty(n, dtype=like.dtype, device=like.device,
+                          pin_memory=like.device.type == "cpu")
     _check16(out, "out")
     if not out.is_contiguous() or out.numel() != n:
         raise ValueError("out must be contiguous with %d elements" % n)
@@ -206,7 +215,8 @@ def head_merge(src: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
     if not src.is_contiguous() or src.numel() != n:
         raise ValueError("src must be contiguous with %d elements" % n)
     if out is None:
-        out = torch.empty((T, H, D), dtype=src.dtype, device=src.device)
+        out = torch.empty((T, H, D), dtype=src.dtype, device=src.device,
+                          pin_memory=src.device.type == "cpu")
     _check16(out, "out")
     if tuple(out.shape) != (T, H, D):
         raise ValueError("out must have shape [T,H,D]")
@@ -230,8 +240,8 @@ def qkv_unpack(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int, outs=
         raise ValueError("recv must be contiguous with %d elements" % n)
     Hp = H // P
     if outs is None:
-        outs = tuple(torch.empty((T, Hp, D), dtype=recv.dtype, device=recv.device)
-                     for _ in range(3))
+        outs = tuple(torch.empty((T, Hp, D), dtype=recv.dtype, device=recv.device,
+                                 pin_memory=recv.device.type == "cpu") for _ in range(3))
     q, k, v = outs
     for t, name in ((q, "q"), (k, "k"), (v, "v")):
         _check16(t, name)

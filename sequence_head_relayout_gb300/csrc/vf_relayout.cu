@@ -164,6 +164,8 @@ int check_pointer(const void *p) {
         return VF_ERR_CUDA;
     }
     if (at.type == cudaMemoryTypeUnregistered) return VF_ERR_ARG;
+    // page-locked host memory must be mapped at the same address on the device
+    if (at.type == cudaMemoryTypeHost && at.devicePointer != p) return VF_ERR_ARG;
     if (at.type == cudaMemoryTypeDevice) {
         int dev = -1;
         if (cudaGetDevice(&dev) != cudaSuccess) {

@@ -188,9 +188,11 @@ def test_piece_table_capacity(L):
     assert L.vf_packed_elems(1, 10, 3, 8, 2, 2) == 240
 
 
-def test_binding_refuses_cpu_tensors(L):
+def test_binding_refuses_pageable_cpu_tensors(L):
     import torch
     with pytest.raises(ValueError):
         vf.qkv_pack(torch.zeros((4, 3, 2, 8), dtype=torch.int16), 2, 1)
     with pytest.raises(ValueError):
         vf.attn_split(torch.zeros((4, 2, 8), dtype=torch.bfloat16), 2, 1)
+    with pytest.raises(ValueError):
+        vf.attn_split(torch.zeros((4, 2, 8), dtype=torch.float32), 2, 1)

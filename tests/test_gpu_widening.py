@@ -221,3 +221,35 @@ def test_gpu_return_exchange_split_merge(shape):
         n_q = sum(length[c * P + q] for c in range(C))
         merged = vf.head_merge(recv, n_q, H, D, P, C)
         assert same_bits(merged, A[min(T, q * shard):min(T, (q + 1) * shard)].contiguous())
+
+
+# --------------------------------------------------------------------------
+# Pinned host memory: the kernels read and write it directly
+# --------------------------------------------------------------------------
+
+def test_pinned_host_zero_copy_all_ops():
+    T, H, D, P, C = 1001, 8, 64, 2, 4
+    Hp = H // P
+    base4 = rand_bits((T, 3 * H * D + 16), 1, device="cpu").pin_memory()   # padded rows
+    hx4 = base4[:, :3 * H * D].unflatten(1, (3, H, D))
+    got = vf.qkv_pack(hx4, P, C)                         # pinned in, pinned out
+    torch.cuda.synchronize()
+    assert got.device.type == "cpu" and got.is_pinned()
+    assert same_bits(got, loops.qkv_pack(hx4, P, C))
+
+    hx3 = rand_bits((H, T, D), 2, device="cpu").pin_memory().permute(1, 0, 2)
+    dev_out = torch.empty(T * H * D, dtype=torch.int16, device=DEV)
+    vf.attn_split(hx3, P, C, out=dev_out)               # pinned in, device out
+    assert same_bits(dev_out, loops.attn_split(hx3, P, C))
+
+    flat = rand_bits((T * H * D,), 3)                   # device in, pinned out
+    hout = torch.zeros((T, H, D), dtype=torch.int16).pin_memory()
+    vf.head_merge(flat, T, H, D, P, C, out=hout)
+    torch.cuda.synchronize()
+    assert same_bits(hout, loops.head_merge(flat.cpu(), T, H, D, P, C))
+
+    recv = rand_bits((3 * T * Hp * D,), 4, device="cpu").pin_memory()
+    q, k, v = vf.qkv_unpack(recv, T, H, D, P, C)
+    torch.cuda.synchronize()
+    for a, b in zip((q, k, v), loops.qkv_unpack_recv(recv, T, H, D, P, C)):
+        assert a.is_pinned() and same_bits(a, b)
