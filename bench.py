@@ -71,7 +71,8 @@ def job_gbs(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> 
 
 def op_elements(cfg):
     T, H, D = cfg.T, cfg.H, cfg.D
-    return {"qkv_pack": 3 * T * H * D, "attn_split": T * H * D, "head_merge": T * H * D}
+    return {"qkv_pack": 3 * T * H * D, "attn_split": T * H * D, "head_merge": T * H * D,
+            "qkv_unpack": 3 * T * (H // cfg.P) * D}
 
 
 def alg_bytes(elems: int) -> int:
@@ -275,6 +276,12 @@ def make_set(cfg, dev, seed_shift, ops=("qkv_pack", "attn_split", "head_merge"))
     if "head_merge" in ops:
         s["merge_src"] = W.merge_source(cfg, device=dev, seed=cfg.seed + seed_shift)
         s["merge_dst"] = torch.empty((cfg.T, cfg.H, cfg.D), dtype=torch.int16, device=dev)
+    if "qkv_unpack" in ops:
+        Hp = cfg.H // cfg.P
+        s["recv"] = torch.empty(3 * cfg.T * Hp * cfg.D, dtype=torch.int16, device=dev)
+        W.fill_(s["recv"], cfg.payload, cfg.seed + seed_shift + 3000)
+        s["qkv_out"] = tuple(torch.empty((cfg.T, Hp, cfg.D), dtype=torch.int16, device=dev)
+                             for _ in range(3))
     return s
 
 
@@ -299,6 +306,11 @@ def run_step(vf, cfg, s, events=None):
         k += 1
         if events:
             events[k].record()
+    if "recv" in s:
+        vf.qkv_unpack(s["recv"], cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, outs=s["qkv_out"])
+        k += 1
+        if events:
+            events[k].record()
 
 
 def launches_per_step(cfg, nops: int) -> int:
@@ -318,8 +330,9 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     vf.lib()
 
-    order = ("qkv_pack", "attn_split", "head_merge")
-    ops_run = tuple(o for o in order if not args.only or o in args.only)
+    order = ("qkv_pack", "attn_split", "head_merge", "qkv_unpack")
+    ops_run = tuple(o for o in order[:3] if not args.only) or tuple(
+        o for o in order if o in args.only)
     sets = [make_set(cfg, dev, 17 * i, ops_run) for i in range(args.sets)]
     torch.cuda.synchronize()
 
@@ -518,7 +531,8 @@ def e2e_arm(args, cfg, dev, world):
         for k in keys_out:
             host[k].copy_(d[k], non_blocking=True)
 
-    step_bytes = sum(alg_bytes(x) for x in op_elements(cfg).values())
+    step_bytes = sum(alg_bytes(op_elements(cfg)[x])
+                     for x in ("qkv_pack", "attn_split", "head_merge"))
     n = max(3, min(args.steps, 20))
 
     def timed(step, streams):
@@ -700,8 +714,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-cores", type=int, default=0)
-    ap.add_argument("--only", nargs="+", choices=["qkv_pack", "attn_split", "head_merge"],
-                    help="time only these relayouts (profiling runs)")
+    ap.add_argument("--only", nargs="+",
+                    choices=["qkv_pack", "attn_split", "head_merge", "qkv_unpack"],
+                    help="time only these relayouts (profiling runs); the receive-side "
+                         "unpack runs only when named here")
     ap.add_argument("--sets", type=int, default=2, help="rotating input/output buffer sets")
     ap.add_argument("--configs", nargs="*", default=["tiny", "4k", "pages", "ragged", "large"],
                     help="workloads for the per-op, per-workload table (none to skip)")

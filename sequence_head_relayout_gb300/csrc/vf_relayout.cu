@@ -25,7 +25,7 @@
 namespace {
 
 #ifndef VF_TARGET_THREADS
-#define VF_TARGET_THREADS 256
+#define VF_TARGET_THREADS 512
 #endif
 constexpr int kTargetThreads = VF_TARGET_THREADS;   // block size aimed at when rows are short
 constexpr int64_t kMaxTablePieces = int64_t(1) << 20;   // P * C limit
