@@ -74,7 +74,8 @@ template <> struct Vec<1> { using T = unsigned short; };
 // stores (evict-first, `.cs`); 1: read-only path loads (`.nc`), plain stores;
 // 2: plain loads and stores.  Measured on GB300 over the pages', ragged and
 // large workloads, 2 is fastest (by about 1%: the streaming hints cost a
-// little and buy nothing when no byte is reused).
+// little and buy nothing when no byte is reused; an L2 256-byte prefetch hint
+// on the loads was no faster either).
 template <typename V>
 __device__ __forceinline__ V load_once(const uint16_t *p) {
 #if VF_CACHE_HINT == 0
@@ -85,6 +86,8 @@ __device__ __forceinline__ V load_once(const uint16_t *p) {
     return *reinterpret_cast<const V *>(p);
 #endif
 }
+
+
 
 template <typename V>
 __device__ __forceinline__ void store_once(uint16_t *p, const V &v) {
