@@ -319,9 +319,12 @@ def run_step(vf, cfg, s, events=None):
             events[k].record()
 
 
-def launches_per_step(cfg, nops: int) -> int:
-    per_launch = 64           # pieces per launch in the library
-    return nops * -(-cfg.P * cfg.C // per_launch)
+def launches_per_step(cfg, ops) -> int:
+    """Kernel launches of one step: one per 128 pieces; a piece is one (chunk,
+    destination) block, times the q/k/v slabs for the pack and the unpack."""
+    per_launch = 128
+    slabs = {"qkv_pack": 3, "qkv_unpack": 3, "attn_split": 1, "head_merge": 1}
+    return sum(-(-slabs[o] * cfg.P * cfg.C // per_launch) for o in ops)
 
 
 def gpu_arm(args, rank, world, local_rank):
@@ -411,6 +414,7 @@ def gpu_arm(args, rank, world, local_rank):
         e2e = e2e_arm(args, cfg, dev, world)
 
     configs = per_config(args, dev) if args.configs else None
+    chain_aba = None if args.no_chain else torch_chain_aba(cfg, dev)
 
     line = None
     if rank == 0:
@@ -432,9 +436,10 @@ def gpu_arm(args, rank, world, local_rank):
             "ops": ops,
             "roofline": roofline,
             "clocks": clock_info,
-            "gpu_launches": K * launches_per_step(cfg, len(ops_run)),
+            "gpu_launches": K * launches_per_step(cfg, ops_run),
             "e2e": e2e,
             "per_config": configs,
+            "vs_torch_chain": chain_aba,
         }
     return line
 
@@ -604,6 +609,117 @@ def e2e_arm(args, cfg, dev, world):
             "mode_description": desc[best], "modes": modes}
 
 
+class TorchChain:
+    """The materialisation chains the direct relayouts replace, on the GPU with
+    PyTorch ops ("Sol-Engine alignment on SM86 and SM89", section "What is
+    enabled": stack/permute/contiguous for the pack, cat/permute/contiguous
+    for the merge; the split copies each token shard's chunk once).  A
+    comparison arm only: the library never runs these."""
+
+    def __init__(self, cfg):
+        import sequence_head_relayout_gb300 as vf
+        self.cfg = cfg
+        T, H, D, P, C = cfg.T, cfg.H, cfg.D, cfg.P, cfg.C
+        self.pack_tab = vf.piece_table(vf.OP_QKV_PACK, T, H, D, P, C)
+        self.split_tab = vf.piece_table(vf.OP_ATTN_SPLIT, T, H, D, P, C)
+        self.merge_tab = vf.piece_table(vf.OP_HEAD_MERGE, T, H, D, P, C)
+
+    def qkv_pack(self, src):
+        import torch
+        cfg = self.cfg
+        P, C, Hp = cfg.P, cfg.C, cfg.H // cfg.P
+        stacked = torch.stack(src.unbind(1))                       # [3, T, H, D]
+        out = torch.empty(3 * cfg.T * cfg.H * cfg.D, dtype=src.dtype, device=src.device)
+        tok, length, off = self.pack_tab
+        for c in range(C):
+            t0, L = tok[c * P], length[c * P]
+            blk = out[off[c * P]:off[c * P] + P * 3 * L * Hp * cfg.D].view(P, 3, L, Hp, cfg.D)
+            blk.copy_(stacked[:, t0:t0 + L].unflatten(2, (P, Hp)).permute(2, 0, 1, 3, 4))
+        return out
+
+    def attn_split(self, src):
+        import torch
+        cfg = self.cfg
+        out = torch.empty(cfg.T * cfg.H * cfg.D, dtype=src.dtype, device=src.device)
+        tok, length, off = self.split_tab
+        for e in range(len(tok)):
+            n = length[e] * cfg.H * cfg.D
+            out[off[e]:off[e] + n].view(length[e], cfg.H, cfg.D).copy_(
+                src[tok[e]:tok[e] + length[e]])
+        return out
+
+    def head_merge(self, flat):
+        import torch
+        cfg = self.cfg
+        P, C, Hp, D = cfg.P, cfg.C, cfg.H // cfg.P, cfg.D
+        tok, length, off = self.merge_tab
+        slabs = [flat[off[c * P]:off[c * P] + P * length[c * P] * Hp * D].view(
+            P, length[c * P], Hp, D) for c in range(C)]
+        slot_major = torch.cat(slabs, 1)                          # [P, T, Hp, D]
+        return slot_major.permute(1, 0, 2, 3).contiguous().view(cfg.T, cfg.H, D)
+
+
+def torch_chain_aba(cfg, dev, reps=20):
+    """A/B/A against the torch chains at one workload: medians of the chain
+    (A, before and after) and of the direct relayout (B), interleaved, each
+    rep after an L2 flush; plus the incremental peak memory of each arm
+    (the pages' allocation screen)."""
+    import torch
+
+    import sequence_head_relayout_gb300 as vf
+    from sequence_head_relayout_gb300 import workloads as W
+
+    chain = TorchChain(cfg)
+    T, H, D, P, C = cfg.T, cfg.H, cfg.D, cfg.P, cfg.C
+    pack_src, _ = W.pack_source(cfg, device=dev)
+    split_src, _ = W.split_source(cfg, device=dev)
+    merge_src = W.merge_source(cfg, device=dev)
+    flush = torch.empty(128 << 20, dtype=torch.int16, device=dev)
+    arms = {
+        "qkv_pack": (lambda: chain.qkv_pack(pack_src), lambda: vf.qkv_pack(pack_src, P, C)),
+        "attn_split": (lambda: chain.attn_split(split_src),
+                       lambda: vf.attn_split(split_src, P, C)),
+        "head_merge": (lambda: chain.head_merge(merge_src),
+                       lambda: vf.head_merge(merge_src, T, H, D, P, C)),
+    }
+    out = {}
+    for op, (a_fn, b_fn) in arms.items():
+        same = torch.equal(a_fn().view(-1), b_fn().view(-1))
+
+        def med(fn):
+            ts = []
+            for _ in range(reps):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                ts.append((e0, e1))
+            torch.cuda.synchronize()
+            return statistics.median(x.elapsed_time(y) for x, y in ts)
+
+        def peak(fn):
+            torch.cuda.synchronize()
+            torch.cuda.reset_peak_memory_stats(dev)
+            base = torch.cuda.memory_allocated(dev)
+            r = fn()
+            torch.cuda.synchronize()
+            p = torch.cuda.max_memory_allocated(dev) - base
+            del r
+            return p
+
+        for _ in range(3):
+            a_fn(), b_fn()
+        a1, b, a2 = med(a_fn), med(b_fn), med(a_fn)
+        out[op] = {"chain_us": [round(a1 * 1e3, 1), round(a2 * 1e3, 1)],
+                   "direct_us": round(b * 1e3, 1),
+                   "speedup": round((a1 + a2) / 2 / b, 3),
+                   "chain_peak_bytes": peak(a_fn), "direct_peak_bytes": peak(b_fn),
+                   "outputs_equal": bool(same)}
+    return out
+
+
 def per_config(args, dev):
     """Median time and effective GB/s of every relayout at every workload.
 
@@ -728,6 +844,8 @@ def main():
     ap.add_argument("--configs", nargs="*", default=["tiny", "4k", "pages", "ragged", "large"],
                     help="workloads for the per-op, per-workload table (none to skip)")
     ap.add_argument("--config-reps", type=int, default=30)
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the A/B/A comparison with the PyTorch materialisation chains")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

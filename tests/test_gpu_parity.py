@@ -263,3 +263,24 @@ def test_host_memory_is_rejected():
     rc = vf.lib().vf_qkv_pack(x4.data_ptr(), (vf._I64 * 4)(*x4.stride()), 4, 2, 8, 2, 1,
                               out.data_ptr(), None)
     assert rc == -1
+
+
+def test_allocation_screen_matches_pages():
+    """The direct relayouts' incremental peak is exactly their output: the
+    figures the pages' allocation screen prints for the direct pack and merge
+    ("Sol-Engine alignment on SM86 and SM89", "What is enabled")."""
+    from tests import _golden
+    g = _golden.load("page_byte_counts.txt")
+    cfg = W.CONFIGS["pages"]
+    src, _ = W.pack_source(cfg, device=DEV)
+    msrc = W.merge_source(cfg, device=DEV)
+    for fn, want in ((lambda: vf.qkv_pack(src, cfg.P, cfg.C), g["pack_direct_bytes"]),
+                     (lambda: vf.head_merge(msrc, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C),
+                      g["merge_direct_bytes"])):
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats(DEV)
+        base = torch.cuda.memory_allocated(DEV)
+        out = fn()
+        torch.cuda.synchronize()
+        assert torch.cuda.max_memory_allocated(DEV) - base == want
+        del out
