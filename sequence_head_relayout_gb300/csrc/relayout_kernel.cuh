@@ -1,4 +1,4 @@
-// Device side of the three relayouts: one row-block copy kernel.
+// Device side of the relayouts: one row-block copy kernel for every op.
 //
 // All the operations ("Sol-Engine alignment on SM86 and SM89", section
 // "What is enabled": QKV destination pack, attention result split,
@@ -58,7 +58,6 @@ struct Args {
     int64_t d_stride;      // strided side, along d (1 on every vector path)
     int32_t heads;         // heads per packed row
     int32_t D;             // elements per head row
-    int32_t npieces;
     int32_t dchunks;       // ceil(D / VW / blockDim.x)
     int32_t z_base;        // first folded z index of this launch (head, d chunks)
     Piece pieces[kMaxPieces];
@@ -86,8 +85,6 @@ __device__ __forceinline__ V load_once(const uint16_t *p) {
     return *reinterpret_cast<const V *>(p);
 #endif
 }
-
-
 
 template <typename V>
 __device__ __forceinline__ void store_once(uint16_t *p, const V &v) {

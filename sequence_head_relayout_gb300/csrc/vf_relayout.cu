@@ -226,7 +226,6 @@ int launch_family(const Plan &pl, cudaStream_t stream) {
             a.pieces[i] = pl.pieces[first + i];
             max_rows = std::max(max_rows, a.pieces[i].rows);
         }
-        a.npieces = int32_t(cnt);
         if (max_rows == 0) continue;
         for (int64_t z0 = 0; z0 < zcount; z0 += kMaxGridZ) {
             a.z_base = int32_t(z0);
@@ -345,6 +344,7 @@ int run(Request rq, cudaStream_t stream) {
     for (int64_t c = rq.c_begin; c < rq.c_end; ++c)
         for (int64_t p = 0; p < s.P; ++p) {
             const Entry &e = table[size_t(c * s.P + p)];
+            if (e.tok_len == 0) continue;             // empty chunk or shard
             // element offset of the block's first row in each slab view; it
             // lies inside the view (checked extent), so it cannot overflow
             const int64_t off = e.tok_start * rq.str[0] + p * group_heads * rq.str[1];
@@ -355,6 +355,7 @@ int run(Request rq, cudaStream_t stream) {
             }
         }
 
+    if (pl.pieces.empty()) return VF_OK;
     const int vw = pick_vector_width(pl);
     const bool packed_is_dst = s.op == VF_OP_QKV_PACK || s.op == VF_OP_ATTN_SPLIT;
     return packed_is_dst ? launch_dir<true>(pl, vw, stream) : launch_dir<false>(pl, vw, stream);

@@ -18,3 +18,11 @@ def pytest_configure(config):
 def oracle_built():
     from oracle import build
     return build.build()
+
+
+@pytest.fixture(scope="session")
+def lib_built():
+    """The CUDA library, built in-tree if missing (nvcc cross-compiles without
+    a GPU); CPU tests use only its host functions."""
+    from sequence_head_relayout_gb300 import _build
+    return _build.build()

@@ -23,9 +23,7 @@ I64 = ctypes.c_int64
 
 
 @pytest.fixture(scope="module")
-def L():
-    from sequence_head_relayout_gb300 import _build
-    _build.build()
+def L(lib_built):
     return vf.lib()
 
 

@@ -7,7 +7,7 @@ import bench
 from oracle import loops
 from sequence_head_relayout_gb300 import workloads as W
 
-pytestmark = pytest.mark.usefixtures("oracle_built")
+pytestmark = pytest.mark.usefixtures("oracle_built", "lib_built")
 
 
 @pytest.mark.parametrize("name", ["tiny", "4k"])
