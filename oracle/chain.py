@@ -87,3 +87,23 @@ def qkv_unpack_recv(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int):
     assert off == flat.numel()
     full = torch.cat([torch.cat(blocks, 1) for blocks in per_rank], 1)   # [3, T, Hp, D]
     return tuple(full[s].contiguous() for s in range(3))
+
+
+def block_lengths(op: int, T: int, H: int, D: int, P: int, C: int):
+    """Element count of every (c, p) block, c outer: a chunk of T (pack,
+    merge) or a chunk of token shard p (split, unpack), times the elements
+    per token."""
+    per_token = {0: 3 * (H // P) * D, 1: H * D, 2: (H // P) * D, 3: 3 * (H // P) * D}[op]
+    if op in (1, 3):
+        shards = part_sizes(T, P)
+        return [[part_sizes(shards[p], C)[c] * per_token for p in range(P)] for c in range(C)]
+    return [[part_sizes(T, C)[c] * per_token for _ in range(P)] for c in range(C)]
+
+
+def to_slot_major(op: int, packed: torch.Tensor, T: int, H: int, D: int, P: int, C: int):
+    """Cut [c][p] storage into its blocks and concatenate them p outer."""
+    flat = _bits(packed).reshape(-1)
+    lens = block_lengths(op, T, H, D, P, C)
+    blocks = list(torch.split(flat, [n for row in lens for n in row]))
+    return torch.cat([blocks[c * P + p] for p in range(P) for c in range(C)]) if blocks \
+        else flat.clone()

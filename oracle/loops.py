@@ -34,6 +34,8 @@ def lib():
             "oracle_qkv_unpack_recv": [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, arr4],
             "oracle_piece_table": [ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
                                    arr4, arr4, arr4, _I64],
+            "oracle_reorder_blocks": [ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _P, _P,
+                                      ctypes.c_int],
         }.items():
             f = getattr(l, name)
             f.argtypes = args
@@ -150,3 +152,23 @@ def piece_table(op: int, T: int, H: int, D: int, P: int, C: int):
     if n != m:
         raise ValueError("oracle_piece_table rejected its arguments")
     return list(a), list(b), list(c)
+
+
+def to_slot_major(op: int, packed: torch.Tensor, T: int, H: int, D: int, P: int,
+                  C: int) -> torch.Tensor:
+    """[c][p] packed storage of ``op`` re-ordered into [p][c] block order."""
+    src = _bits(packed).contiguous()
+    out = torch.empty_like(src)
+    n = lib().oracle_reorder_blocks(op, T, H, D, P, C, src.data_ptr(), out.data_ptr(), 1)
+    _check(n, src.numel(), "reorder_blocks")
+    return out
+
+
+def to_chunk_major(op: int, packed: torch.Tensor, T: int, H: int, D: int, P: int,
+                   C: int) -> torch.Tensor:
+    """[p][c] packed storage of ``op`` re-ordered into [c][p] block order."""
+    src = _bits(packed).contiguous()
+    out = torch.empty_like(src)
+    n = lib().oracle_reorder_blocks(op, T, H, D, P, C, src.data_ptr(), out.data_ptr(), 0)
+    _check(n, src.numel(), "reorder_blocks")
+    return out

@@ -304,3 +304,57 @@ int64_t oracle_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, i
         }
     return e;
 }
+
+/* ---- slot-major block order ------------------------------------------- */
+
+/*
+ * Block order variant: storage [p][c] (all chunks of destination p, then
+ * destination p+1) instead of [c][p].  Reading of the layout-variant row of
+ * the build plan; the pages' own storage is the four-chunk overlap layout,
+ * chunk blocks outermost.  Because the blocks are the same and only their
+ * order changes, the oracle for every op in this order is the [c][p] oracle
+ * composed with this block permutation: block (c, p) of `cp` (sizes and
+ * offsets from oracle_piece_table's cursor walk) is copied to the next free
+ * place of `pc`, walking p outer and c inner.  `to_slot_major` = 0 copies
+ * the other way ([p][c] storage back to [c][p]).  Returns elements copied.
+ */
+int64_t oracle_reorder_blocks(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                              const uint16_t *from, uint16_t *to, int to_slot_major) {
+    if (bad_dims(T, H, D, P, C)) return -1;
+    if (op != 1 && (H % P != 0)) return -1;
+    int64_t per_token;
+    if (op == 0) per_token = 3 * (H / P) * D;
+    else if (op == 1) per_token = H * D;
+    else if (op == 2) per_token = (H / P) * D;
+    else if (op == 3) per_token = 3 * (H / P) * D;
+    else return -1;
+    int64_t k = 0;
+    for (int64_t p = 0; p < P; ++p)
+        for (int64_t c = 0; c < C; ++c) {
+            /* offset and length of block (c, p) in [c][p] order */
+            int64_t off = 0, len = 0;
+            for (int64_t cc = 0; cc <= c; ++cc)
+                for (int64_t pp = 0; pp < P; ++pp) {
+                    int64_t n;
+                    if (op == 1 || op == 3) {
+                        const int64_t a = part_begin(T, P, pp);
+                        const int64_t m = part_end(T, P, pp) - a;
+                        n = part_end(m, C, cc) - part_begin(m, C, cc);
+                    } else {
+                        n = part_end(T, C, cc) - part_begin(T, C, cc);
+                    }
+                    if (cc == c && pp == p) {
+                        len = n * per_token;
+                        goto found;
+                    }
+                    off += n * per_token;
+                }
+        found:
+            for (int64_t i = 0; i < len; ++i) {
+                if (to_slot_major) to[k + i] = from[off + i];
+                else to[off + i] = from[k + i];
+            }
+            k += len;
+        }
+    return k;
+}

@@ -458,3 +458,46 @@ def test_pins_catch_planted_unpack_mistake():
     recv = iota((30,))
     q, _, _ = unpack_global_quota(recv, 5, 4, 1, 2, 2)
     assert q.reshape(-1).tolist() != g["expected_q"]
+
+
+# --------------------------------------------------------------------------
+# 10. Slot-major ([p][c]) block order
+# --------------------------------------------------------------------------
+
+def test_golden_slot_major_pack():
+    g = _golden.load("slotmajor_pack_T3_H4_D2_P2_C2.txt")
+    T, H, D, P, C = g["T"], g["H"], g["D"], g["P"], g["C"]
+    cp = loops.qkv_pack(iota((T, 3, H, D)), P, C)
+    assert loops.to_slot_major(0, cp, T, H, D, P, C).tolist() == g["expected"]
+    assert chain.to_slot_major(0, cp, T, H, D, P, C).tolist() == g["expected"]
+
+
+@pytest.mark.parametrize("shape", [(7, 6, 5, 3, 4), (55, 8, 2, 4, 4), (5, 4, 2, 4, 2),
+                                   (1, 2, 3, 2, 5), (0, 2, 2, 2, 2)])
+def test_slot_major_library_reductions(shape):
+    T, H, D, P, C = shape
+    x3 = rand_bits((T, H, D), 3)
+    # the split's shards are consecutive token ranges and a shard's chunks are
+    # consecutive too: in slot-major order the split is a contiguous copy
+    pc = loops.to_slot_major(1, loops.attn_split(x3, P, C), T, H, D, P, C)
+    assert bits_equal(pc, x3.reshape(-1))
+    # a slot-major merge source holds head group p of every token at slot p:
+    # it is a [P][T][H/P][D] tensor and the merge is a permute
+    flat = rand_bits((T * H * D,), 4)
+    cp = loops.to_chunk_major(2, flat, T, H, D, P, C)
+    merged = loops.head_merge(cp, T, H, D, P, C)
+    assert bits_equal(merged, flat.view(P, T, H // P, D).permute(1, 0, 2, 3).reshape(T, H, D))
+
+
+@pytest.mark.parametrize("op", [0, 1, 2, 3])
+@pytest.mark.parametrize("shape", [(33, 6, 8, 3, 4), (7, 8, 3, 8, 16), (100, 12, 2, 4, 7),
+                                   (9, 4, 5, 2, 1)])
+def test_reorder_loops_agree_with_chain_and_invert(op, shape):
+    T, H, D, P, C = shape
+    n = {0: 3 * T * H * D, 1: T * H * D, 2: T * H * D, 3: 3 * T * (H // P) * D}[op]
+    cp = rand_bits((n,), op + 40)
+    pc = loops.to_slot_major(op, cp, T, H, D, P, C)
+    assert bits_equal(pc, chain.to_slot_major(op, cp, T, H, D, P, C))
+    assert bits_equal(loops.to_chunk_major(op, pc, T, H, D, P, C), cp)
+    if C == 1 or P == 1:                      # one index: both orders coincide
+        assert bits_equal(pc, cp)
