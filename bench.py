@@ -758,6 +758,10 @@ def per_config(args, dev):
                                                                  outs=outs)),
             "qkv_pack3": (3 * T * H * D, lambda: vf.qkv_pack3(
                 pack_src[:, 0], pack_src[:, 1], pack_src[:, 2], P, C, out=pack_dst)),
+            "qkv_pack_slot_major": (3 * T * H * D, lambda: vf.qkv_pack(
+                pack_src, P, C, out=pack_dst, order="slot_major")),
+            "head_merge_slot_major": (T * H * D, lambda: vf.head_merge(
+                merge_src, T, H, D, P, C, out=merge_dst, order="slot_major")),
         }
         row = {}
         for op, (elems, fn) in ops.items():

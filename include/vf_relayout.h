@@ -84,6 +84,16 @@ typedef enum vf_op {
     VF_OP_QKV_UNPACK = 3
 } vf_op;
 
+/* Order of the (c, p) blocks in packed storage.  Chunk-major is the
+ * four-chunk overlap layout of the pages (each chunk's exchange input is one
+ * contiguous P-slot slab) and the order of every entry point except
+ * vf_relayout.  Slot-major keeps all chunks of one destination together
+ * (one contiguous span per destination for a single, unchunked exchange). */
+typedef enum vf_order {
+    VF_ORDER_CHUNK_MAJOR = 0,   /* [c][p] */
+    VF_ORDER_SLOT_MAJOR = 1     /* [p][c] */
+} vf_order;
+
 /*
  * QKV destination pack.  ("Sol-Engine alignment on SM86 and SM89", "What is
  * enabled": QKV destination pack; the source is the merged QKV projection's
@@ -206,6 +216,36 @@ int vf_qkv_pack3(const void *q, const void *k, const void *v, const int64_t qkv_
                  int64_t c_begin, int64_t c_count, void *dst, vf_stream_t stream);
 
 /*
+ * General form of every operation above, with the block order as a field.
+ * The named entry points are this call with order = VF_ORDER_CHUNK_MAJOR.
+ *
+ * op, order:   vf_op, vf_order.
+ * T..C:        as for the named entry points (the unpack takes the global T
+ *              and H, as vf_qkv_unpack does).
+ * c_begin, c_count: chunks to move, (0, C) for all.
+ * packed:      the packed storage (written by the pack and the split, read
+ *              by the merge and the unpack), in `order`.
+ * strided:     the strided-side views, all with the element strides
+ *              `strides` (token, head, d): pack -> q, k, v [T][H][D] (read;
+ *              for a fused [T][3][H][D] view pass its three slab bases);
+ *              split -> [0] = [T][H][D] (read); merge -> [0] = [T][H][D]
+ *              (written); unpack -> q, k, v [T][H/P][D] (written).  Entries
+ *              past the op's slab count are ignored.
+ * Errors as for the named entry points; an unknown order is VF_ERR_ARG.
+ */
+typedef struct vf_relayout_desc {
+    int32_t op;
+    int32_t order;
+    int64_t T, H, D, P, C;
+    int64_t c_begin, c_count;
+    void *packed;
+    void *strided[3];
+    int64_t strides[3];
+} vf_relayout_desc;
+
+int vf_relayout(const vf_relayout_desc *desc, vf_stream_t stream);
+
+/*
  * Number of elements of the packed side of `op` (3*T*H*D for the pack,
  * T*H*D for the split and the merge, 3*T*(H/P)*D for the unpack), or a
  * negative vf_status on bad arguments or overflow.  Pure host function.
@@ -213,17 +253,23 @@ int vf_qkv_pack3(const void *q, const void *k, const void *v, const int64_t qkv_
 int64_t vf_packed_elems(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C);
 
 /*
- * The piece table of `op`: for each (c, p) in storage order (c outer), the
- * first token (tok_start; for the split and the unpack, counted in the
- * strided view's token numbering, so shard p's chunk c), the token count
- * (tok_len) and the element offset of the block in packed storage
- * (packed_off).  For the unpack, p is the source rank.  Writes C*P entries into each caller-owned
- * array of capacity `cap` and returns C*P, or a negative vf_status
- * (VF_ERR_CAPACITY when cap < C*P).  Pure host function.
+ * The piece table of `op`: entry c*P + p describes block (c, p): the first
+ * token (tok_start; for the split and the unpack, counted in the strided
+ * view's token numbering, so shard p's chunk c), the token count (tok_len)
+ * and the element offset of the block in packed storage (packed_off) for
+ * chunk-major storage.  For the unpack, p is the source rank.  Writes C*P
+ * entries into each caller-owned array of capacity `cap` and returns C*P, or
+ * a negative vf_status (VF_ERR_CAPACITY when cap < C*P).  Pure host function.
  */
 int64_t vf_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
                        int64_t *tok_start, int64_t *tok_len, int64_t *packed_off,
                        int64_t cap);
+
+/* vf_piece_table with the block order given: entries are still indexed
+ * c*P + p; packed_off places the blocks in `order` (vf_order). */
+int64_t vf_piece_table_ex(int op, int order, int64_t T, int64_t H, int64_t D, int64_t P,
+                          int64_t C, int64_t *tok_start, int64_t *tok_len,
+                          int64_t *packed_off, int64_t cap);
 
 /* Static, NUL-terminated description of a vf_status value. */
 const char *vf_status_string(int status);

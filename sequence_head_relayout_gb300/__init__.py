@@ -20,7 +20,9 @@ enabled"):
 * :func:`qkv_pack3`  -- the pack from three separate Q, K, V views.
 
 Every function takes ``chunks=(c_begin, c_count)`` to move only those overlap
-chunks (the packed buffer is always the full one).
+chunks (the packed buffer is always the full one) and ``order`` for the block
+order of the packed storage: ``"chunk_major"`` ([c][p], the four-chunk overlap
+layout, default) or ``"slot_major"`` ([p][c]).
 """
 import ctypes
 import os
@@ -32,6 +34,7 @@ __all__ = ["qkv_pack", "qkv_pack3", "attn_split", "head_merge", "qkv_unpack", "p
            "OP_QKV_UNPACK"]
 
 OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE, OP_QKV_UNPACK = 0, 1, 2, 3
+ORDERS = {"chunk_major": 0, "slot_major": 1}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libvf_relayout.so")
@@ -40,6 +43,14 @@ _lib = None
 _I64 = ctypes.c_int64
 _P = ctypes.c_void_p
 _I64P = ctypes.POINTER(_I64)
+
+
+class _Desc(ctypes.Structure):
+    """vf_relayout_desc of the C ABI."""
+    _fields_ = [("op", ctypes.c_int32), ("order", ctypes.c_int32),
+                ("T", _I64), ("H", _I64), ("D", _I64), ("P", _I64), ("C", _I64),
+                ("c_begin", _I64), ("c_count", _I64), ("packed", _P),
+                ("strided", _P * 3), ("strides", _I64 * 3)]
 
 
 class VFError(RuntimeError):
@@ -79,6 +90,11 @@ def lib():
         l.vf_piece_table.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
                                      _I64P, _I64P, _I64P, _I64]
         l.vf_piece_table.restype = _I64
+        l.vf_piece_table_ex.argtypes = [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64, _I64,
+                                        _I64, _I64P, _I64P, _I64P, _I64]
+        l.vf_piece_table_ex.restype = _I64
+        l.vf_relayout.argtypes = [ctypes.POINTER(_Desc), _P]
+        l.vf_relayout.restype = ctypes.c_int
         l.vf_status_string.argtypes = [ctypes.c_int]
         l.vf_status_string.restype = ctypes.c_char_p
         _lib = l
@@ -117,18 +133,26 @@ def _call(fn, *args):
 
 
 def packed_elems(op: int, T: int, H: int, D: int, P: int, C: int) -> int:
-    """Elements of the packed side of ``op`` (3*T*H*D for the pack, else T*H*D)."""
+    """Elements of the packed side of ``op`` (3*T*H*D for the pack, T*H*D for the
+    split and the merge, 3*T*(H/P)*D for the unpack)."""
     n = lib().vf_packed_elems(op, T, H, D, P, C)
     if n < 0:
         raise VFError("vf_packed_elems", n)
     return n
 
 
-def piece_table(op: int, T: int, H: int, D: int, P: int, C: int):
-    """(tok_start, tok_len, packed_off) lists over (c, p) blocks in storage order."""
+def _order(order) -> int:
+    if order not in ORDERS:
+        raise ValueError("order must be one of %s" % sorted(ORDERS))
+    return ORDERS[order]
+
+
+def piece_table(op: int, T: int, H: int, D: int, P: int, C: int, order="chunk_major"):
+    """(tok_start, tok_len, packed_off) lists; entry c*P + p is block (c, p),
+    packed_off places the blocks in the given storage order."""
     m = P * C
     a, b, c = (_I64 * m)(), (_I64 * m)(), (_I64 * m)()
-    n = lib().vf_piece_table(op, T, H, D, P, C, a, b, c, m)
+    n = lib().vf_piece_table_ex(op, _order(order), T, H, D, P, C, a, b, c, m)
     if n < 0:
         raise VFError("vf_piece_table", n)
     return list(a), list(b), list(c)
@@ -136,6 +160,20 @@ def piece_table(op: int, T: int, H: int, D: int, P: int, C: int):
 
 def _range(chunks, C):
     return (0, C) if chunks is None else (int(chunks[0]), int(chunks[1]))
+
+
+def _relayout(op, order, T, H, D, P, C, chunks, packed, strided, strides, stream):
+    """vf_relayout with a descriptor (the general entry, any block order)."""
+    c0, cn = _range(chunks, C)
+    d = _Desc(op=op, order=order, T=T, H=H, D=D, P=P, C=C, c_begin=c0, c_count=cn,
+              packed=packed)
+    for i, ptr in enumerate(strided):
+        d.strided[i] = ptr
+    for i, st in enumerate(strides):
+        d.strides[i] = st
+    rc = lib().vf_relayout(ctypes.byref(d), stream)
+    if rc != 0:
+        raise VFError("vf_relayout", rc)
 
 
 def _flat_out(out, n, like):
@@ -149,7 +187,8 @@ def _flat_out(out, n, like):
 
 
 def qkv_pack(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
-             stream: torch.cuda.Stream = None, chunks=None) -> torch.Tensor:
+             stream: torch.cuda.Stream = None, chunks=None,
+             order="chunk_major") -> torch.Tensor:
     """QKV destination pack of a [T,3,H,D] CUDA view (any strides).
 
     Returns (or fills) a flat tensor of 3*T*H*D elements: blocks (c, p) in
@@ -160,6 +199,13 @@ def qkv_pack(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
         raise ValueError("src must be a [T,3,H,D] view")
     T, _, H, D = src.shape
     out = _flat_out(out, packed_elems(OP_QKV_PACK, T, H, D, P, C), src)
+    o = _order(order)
+    if o:
+        st = src.stride()
+        bases = [src.data_ptr() + s * st[1] * src.element_size() for s in range(3)]
+        _relayout(OP_QKV_PACK, o, T, H, D, P, C, chunks, out.data_ptr(), bases,
+                  (st[0], st[2], st[3]), _stream(stream, src.device))
+        return out
     c0, cn = _range(chunks, C)
     _call("vf_qkv_pack_chunks", src.data_ptr(), _strides(src), T, H, D, P, C, c0, cn,
           out.data_ptr(), _stream(stream, src.device))
@@ -168,7 +214,7 @@ def qkv_pack(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
 
 def qkv_pack3(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, C: int,
               out: torch.Tensor = None, stream: torch.cuda.Stream = None,
-              chunks=None) -> torch.Tensor:
+              chunks=None, order="chunk_major") -> torch.Tensor:
     """QKV destination pack from three [T,H,D] CUDA views with equal strides."""
     for t, name in ((q, "q"), (k, "k"), (v, "v")):
         _check16(t, name)
@@ -178,6 +224,12 @@ def qkv_pack3(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, C: int,
         raise ValueError("q, k, v must share their strides")
     T, H, D = q.shape
     out = _flat_out(out, packed_elems(OP_QKV_PACK, T, H, D, P, C), q)
+    o = _order(order)
+    if o:
+        _relayout(OP_QKV_PACK, o, T, H, D, P, C, chunks, out.data_ptr(),
+                  [q.data_ptr(), k.data_ptr(), v.data_ptr()], q.stride(),
+                  _stream(stream, q.device))
+        return out
     c0, cn = _range(chunks, C)
     _call("vf_qkv_pack3", q.data_ptr(), k.data_ptr(), v.data_ptr(), _strides(q), T, H, D, P,
           C, c0, cn, out.data_ptr(), _stream(stream, q.device))
@@ -185,7 +237,8 @@ def qkv_pack3(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, C: int,
 
 
 def attn_split(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
-               stream: torch.cuda.Stream = None, chunks=None) -> torch.Tensor:
+               stream: torch.cuda.Stream = None, chunks=None,
+               order="chunk_major") -> torch.Tensor:
     """Attention-result split of a [T,H,D] CUDA view (any strides).
 
     Returns (or fills) a flat tensor of T*H*D elements: blocks (c, p) in
@@ -196,6 +249,11 @@ def attn_split(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
         raise ValueError("src must be a [T,H,D] view")
     T, H, D = src.shape
     out = _flat_out(out, packed_elems(OP_ATTN_SPLIT, T, H, D, P, C), src)
+    o = _order(order)
+    if o:
+        _relayout(OP_ATTN_SPLIT, o, T, H, D, P, C, chunks, out.data_ptr(), [src.data_ptr()],
+                  src.stride(), _stream(stream, src.device))
+        return out
     c0, cn = _range(chunks, C)
     _call("vf_attn_split_chunks", src.data_ptr(), _strides(src), T, H, D, P, C, c0, cn,
           out.data_ptr(), _stream(stream, src.device))
@@ -204,7 +262,7 @@ def attn_split(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
 
 def head_merge(src: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
                out: torch.Tensor = None, stream: torch.cuda.Stream = None,
-               chunks=None) -> torch.Tensor:
+               chunks=None, order="chunk_major") -> torch.Tensor:
     """Returned-head merge of a flat received buffer into a [T,H,D] view.
 
     ``out`` may be any non-overlapping strided [T,H,D] CUDA view; a
@@ -220,6 +278,11 @@ def head_merge(src: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
     _check16(out, "out")
     if tuple(out.shape) != (T, H, D):
         raise ValueError("out must have shape [T,H,D]")
+    o = _order(order)
+    if o:
+        _relayout(OP_HEAD_MERGE, o, T, H, D, P, C, chunks, src.data_ptr(), [out.data_ptr()],
+                  out.stride(), _stream(stream, src.device))
+        return out
     c0, cn = _range(chunks, C)
     _call("vf_head_merge_chunks", src.data_ptr(), _strides(out), T, H, D, P, C, c0, cn,
           out.data_ptr(), _stream(stream, src.device))
@@ -227,7 +290,7 @@ def head_merge(src: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
 
 
 def qkv_unpack(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int, outs=None,
-               stream: torch.cuda.Stream = None, chunks=None):
+               stream: torch.cuda.Stream = None, chunks=None, order="chunk_major"):
     """Receive-side QKV unpack: flat received buffer of 3*T*(H/P)*D elements
     into (Q, K, V), each a [T, H/P, D] view (global token order).
 
@@ -249,6 +312,12 @@ def qkv_unpack(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int, outs=
             raise ValueError("%s must have shape [T,H/P,D]" % name)
     if q.stride() != k.stride() or q.stride() != v.stride():
         raise ValueError("q, k, v must share their strides")
+    o = _order(order)
+    if o:
+        _relayout(OP_QKV_UNPACK, o, T, H, D, P, C, chunks, recv.data_ptr(),
+                  [q.data_ptr(), k.data_ptr(), v.data_ptr()], q.stride(),
+                  _stream(stream, recv.device))
+        return outs
     c0, cn = _range(chunks, C)
     _call("vf_qkv_unpack_chunks", recv.data_ptr(), T, H, D, P, C, c0, cn, q.data_ptr(),
           k.data_ptr(), v.data_ptr(), _strides(q), _stream(stream, recv.device))

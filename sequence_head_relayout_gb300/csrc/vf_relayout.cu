@@ -87,30 +87,39 @@ struct Entry {
     int64_t tok_start, tok_len, packed_off;
 };
 
-// Piece table in storage order (c outer, p inner).  Requires check_shape OK.
-// Pack and merge cut the T tokens of this rank into chunks; the split and the
-// unpack cut T into P token shards first and each shard into chunks.
-std::vector<Entry> piece_table(const Shape &s) {
-    std::vector<Entry> out;
-    out.reserve(size_t(s.P * s.C));
+// Piece table, one entry per (c, p) at index c * P + p.  Pack and merge cut
+// the T tokens of this rank into chunks; the split and the unpack cut T into
+// P token shards first and each shard into chunks.  packed_off places the
+// blocks back to back in the requested storage order: c outer (chunk-major,
+// the overlap layout) or p outer (slot-major).  Requires check_shape OK.
+std::vector<Entry> piece_table(const Shape &s, int order) {
+    std::vector<Entry> out(size_t(s.P * s.C));
     const int64_t per_token = slabs_of(s.op) * heads_per_row(s) * s.D;
     const bool sharded = s.op == VF_OP_ATTN_SPLIT || s.op == VF_OP_QKV_UNPACK;
-    int64_t cursor = 0;                                     // packed elements
     for (int64_t c = 0; c < s.C; ++c)
         for (int64_t p = 0; p < s.P; ++p) {
-            int64_t first, len;
+            Entry &e = out[size_t(c * s.P + p)];
             if (sharded) {
                 const int64_t a = part_begin(s.T, s.P, p);
                 const int64_t n = part_begin(s.T, s.P, p + 1) - a;
                 const int64_t u0 = part_begin(n, s.C, c);
-                first = a + u0;
-                len = part_begin(n, s.C, c + 1) - u0;
+                e.tok_start = a + u0;
+                e.tok_len = part_begin(n, s.C, c + 1) - u0;
             } else {
-                first = part_begin(s.T, s.C, c);
-                len = part_begin(s.T, s.C, c + 1) - first;
+                e.tok_start = part_begin(s.T, s.C, c);
+                e.tok_len = part_begin(s.T, s.C, c + 1) - e.tok_start;
             }
-            out.push_back({first, len, cursor});
-            cursor += len * per_token;
+        }
+    int64_t cursor = 0;                                     // packed elements
+    const int64_t outer = order == VF_ORDER_SLOT_MAJOR ? s.P : s.C;
+    const int64_t inner = order == VF_ORDER_SLOT_MAJOR ? s.C : s.P;
+    for (int64_t i = 0; i < outer; ++i)
+        for (int64_t j = 0; j < inner; ++j) {
+            const int64_t c = order == VF_ORDER_SLOT_MAJOR ? j : i;
+            const int64_t p = order == VF_ORDER_SLOT_MAJOR ? i : j;
+            Entry &e = out[size_t(c * s.P + p)];
+            e.packed_off = cursor;
+            cursor += e.tok_len * per_token;
         }
     return out;
 }
@@ -180,6 +189,7 @@ int check_pointer(const void *p) {
 // One call, after the entry point has mapped its arguments.
 struct Request {
     Shape s;
+    int order;                     // vf_order of the packed storage
     int64_t c_begin, c_end;        // chunk range [c_begin, c_end)
     void *packed;                  // packed storage (read for merge/unpack)
     const void *strided[3];        // strided-side base per slab
@@ -278,6 +288,7 @@ int run(Request rq, cudaStream_t stream) {
     int rc = check_shape(s);
     if (rc != VF_OK) return rc;
     if (rq.c_begin < 0 || rq.c_end < rq.c_begin || rq.c_end > s.C) return VF_ERR_ARG;
+    if (rq.order != VF_ORDER_CHUNK_MAJOR && rq.order != VF_ORDER_SLOT_MAJOR) return VF_ERR_ARG;
     const int64_t slabs = slabs_of(s.op);
 
     // Geometry of one strided slab view [T][heads_view][D].
@@ -337,7 +348,7 @@ int run(Request rq, cudaStream_t stream) {
     // address head group p of a full-head view; the split and the unpack
     // address all heads of their view.  A pack or unpack block holds its
     // q, k, v slabs back to back, each rows x heads x D.
-    const std::vector<Entry> table = piece_table(s);
+    const std::vector<Entry> table = piece_table(s, rq.order);
     const int64_t group_heads = (s.op == VF_OP_QKV_PACK || s.op == VF_OP_HEAD_MERGE)
                                     ? s.H / s.P : 0;
     const int64_t R = pl.heads * pl.D;
@@ -531,21 +542,47 @@ int64_t vf_packed_elems(int op, int64_t T, int64_t H, int64_t D, int64_t P, int6
     return rc != VF_OK ? rc : packed_elems(s);
 }
 
-int64_t vf_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
-                       int64_t *tok_start, int64_t *tok_len, int64_t *packed_off,
-                       int64_t cap) {
+int64_t vf_piece_table_ex(int op, int order, int64_t T, int64_t H, int64_t D, int64_t P,
+                          int64_t C, int64_t *tok_start, int64_t *tok_len,
+                          int64_t *packed_off, int64_t cap) {
     const Shape s{op, T, H, D, P, C};
     const int rc = check_shape(s);
     if (rc != VF_OK) return rc;
+    if (order != VF_ORDER_CHUNK_MAJOR && order != VF_ORDER_SLOT_MAJOR) return VF_ERR_ARG;
     if (cap < P * C) return VF_ERR_CAPACITY;
     if (!tok_start || !tok_len || !packed_off) return VF_ERR_ARG;
-    const std::vector<Entry> t = piece_table(s);
+    const std::vector<Entry> t = piece_table(s, order);
     for (size_t i = 0; i < t.size(); ++i) {
         tok_start[i] = t[i].tok_start;
         tok_len[i] = t[i].tok_len;
         packed_off[i] = t[i].packed_off;
     }
     return int64_t(t.size());
+}
+
+int64_t vf_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                       int64_t *tok_start, int64_t *tok_len, int64_t *packed_off,
+                       int64_t cap) {
+    return vf_piece_table_ex(op, VF_ORDER_CHUNK_MAJOR, T, H, D, P, C, tok_start, tok_len,
+                             packed_off, cap);
+}
+
+int vf_relayout(const vf_relayout_desc *d, vf_stream_t stream) {
+    if (d == nullptr) return VF_ERR_ARG;
+    Request rq{};
+    rq.s = {d->op, d->T, d->H, d->D, d->P, d->C};
+    if (!is_op(d->op)) return VF_ERR_ARG;
+    rq.order = d->order;
+    rq.c_begin = d->c_begin;
+    rq.c_end = range_end(d->c_begin, d->c_count);
+    rq.packed = d->packed;
+    const int64_t slabs = slabs_of(d->op);
+    for (int i = 0; i < 3; ++i) rq.strided[i] = i < slabs ? d->strided[i] : nullptr;
+    for (int i = 0; i < 3; ++i) rq.str[i] = d->strides[i];
+    if (d->P < 1 || d->H < 0) return VF_ERR_ARG;
+    rq.heads_view = d->op == VF_OP_QKV_UNPACK ? d->H / d->P : d->H;
+    rq.strided_written = d->op == VF_OP_HEAD_MERGE || d->op == VF_OP_QKV_UNPACK;
+    return run(rq, as_stream(stream));
 }
 
 const char *vf_status_string(int status) {

@@ -194,3 +194,45 @@ def test_binding_refuses_pageable_cpu_tensors(L):
         vf.attn_split(torch.zeros((4, 2, 8), dtype=torch.bfloat16), 2, 1)
     with pytest.raises(ValueError):
         vf.attn_split(torch.zeros((4, 2, 8), dtype=torch.float32), 2, 1)
+
+
+@pytest.mark.parametrize("shape", [(55413, 32, 64, 4, 4), (37, 6, 16, 3, 7), (5, 4, 2, 4, 2),
+                                   (0, 2, 2, 2, 3)])
+def test_slot_major_piece_tables(L, shape):
+    """Slot-major offsets are the chunk-major blocks (lengths from the oracle's
+    table) laid out p outer, c inner."""
+    T, H, D, P, C = shape
+    for op in (0, 1, 2, 3):
+        tok, length, _ = loops.piece_table(op, T, H, D, P, C)
+        per = {0: 3 * (H // P) * D, 1: H * D, 2: (H // P) * D, 3: 3 * (H // P) * D}[op]
+        want, cur = [0] * (P * C), 0
+        for p in range(P):
+            for c in range(C):
+                want[c * P + p] = cur
+                cur += length[c * P + p] * per
+        got = vf.piece_table(op, T, H, D, P, C, order="slot_major")
+        assert got[0] == tok and got[1] == length and got[2] == want
+
+
+def test_relayout_descriptor_rejections(L):
+    d = vf._Desc(op=0, order=0, T=4, H=4, D=8, P=2, C=2, c_begin=0, c_count=2,
+                 packed=FAKE_DST)
+    for i in range(3):
+        d.strided[i] = FAKE_SRC + 4096 * i
+    d.strides[0], d.strides[1], d.strides[2] = 32, 8, 1
+    assert L.vf_relayout(None, None) == -1
+    d.order = 2
+    assert L.vf_relayout(ctypes.byref(d), None) == -1
+    d.order, d.op = 1, 7
+    assert L.vf_relayout(ctypes.byref(d), None) == -1
+    d.op, d.P = 0, 3
+    assert L.vf_relayout(ctypes.byref(d), None) == -1            # H % P
+    d.P, d.c_count = 2, 0
+    assert L.vf_relayout(ctypes.byref(d), None) == 0             # nothing to move
+    d.c_count, d.packed = 2, FAKE_SRC + 8
+    assert L.vf_relayout(ctypes.byref(d), None) == -3            # packed overlaps q
+    d.op, d.packed = 3, FAKE_DST                                 # unpack writes q, k, v
+    d.strided[1] = d.strided[0]
+    assert L.vf_relayout(ctypes.byref(d), None) == -3            # outputs alias
+    assert L.vf_piece_table_ex(0, 5, 4, 4, 8, 2, 2, _i64(0, 0, 0, 0), _i64(0, 0, 0, 0),
+                               _i64(0, 0, 0, 0), 4) == -1

@@ -100,9 +100,14 @@ def test_fuzz_all_ops(seed):
     # three-pointer pack from the slabs of the same view
     assert torch.equal(vf.qkv_pack3(x4[:, 0], x4[:, 1], x4[:, 2], P, C).cpu(), want)
 
-    # split
+    # split, in both block orders
     x3 = view_of((T, H, D), layout, offset, rng)
-    assert torch.equal(vf.attn_split(x3, P, C).cpu(), loops.attn_split(x3.cpu(), P, C))
+    want3 = loops.attn_split(x3.cpu(), P, C)
+    assert torch.equal(vf.attn_split(x3, P, C).cpu(), want3)
+    assert torch.equal(vf.attn_split(x3, P, C, order="slot_major").cpu(),
+                       loops.to_slot_major(1, want3, T, H, D, P, C))
+    assert torch.equal(vf.qkv_pack(x4, P, C, order="slot_major").cpu(),
+                       loops.to_slot_major(0, want, T, H, D, P, C))
 
     # merge into a strided destination (never broadcast)
     flat = rand_bits(T * H * D, rng).to(DEV)
