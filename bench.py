@@ -15,7 +15,7 @@ region, an end-to-end figure through the public API with pinned host buffers
 (host-to-device copies of the inputs and device-to-host copies of the
 outputs inside the timed region), and the CPU oracle timed on host cores.
 
-``--impl reference``: the CPU oracle as it stands, on the host cores, timed
+``--impl reference``: the CPU oracle, unmodified, on the host cores, timed
 on a bounded token sample of the same workload each step.
 
 Several GPUs (torchrun): every rank runs an independent replica of the

@@ -309,9 +309,9 @@ int64_t oracle_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, i
 
 /*
  * Block order variant: storage [p][c] (all chunks of destination p, then
- * destination p+1) instead of [c][p].  Reading of the layout-variant row of
- * the build plan; the pages' own storage is the four-chunk overlap layout,
- * chunk blocks outermost.  Because the blocks are the same and only their
+ * destination p+1) instead of [c][p].  The pages' own storage is the
+ * four-chunk overlap layout, chunk blocks outermost; this variant keeps each
+ * destination's blocks in one span.  Because the blocks are the same and only their
  * order changes, the oracle for every op in this order is the [c][p] oracle
  * composed with this block permutation: block (c, p) of `cp` (sizes and
  * offsets from oracle_piece_table's cursor walk) is copied to the next free
