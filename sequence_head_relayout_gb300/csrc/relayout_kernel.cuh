@@ -39,6 +39,7 @@ namespace vf {
 #define VF_CACHE_HINT 2
 #endif
 
+
 constexpr int kMaxPieces = 128;                    // pieces per launch (parameter space)
 constexpr int kRowsPerThread = VF_ROWS_PER_THREAD; // independent loads in flight per thread
 constexpr int kMaxThreads = 512;                   // threads per block, upper bound
@@ -60,6 +61,7 @@ struct Args {
     int32_t D;             // elements per head row
     int32_t dchunks;       // ceil(D / VW / blockDim.x)
     int32_t z_base;        // first folded z index of this launch (head, d chunks)
+    int32_t piece_fastest; // grid x walks pieces and y row groups (else the reverse)
     Piece pieces[kMaxPieces];
 };
 
@@ -95,18 +97,20 @@ __device__ __forceinline__ void store_once(uint16_t *p, const V &v) {
 #endif
 }
 
-// Grid: x = groups of kRowsPerThread * blockDim.z rows, y = piece,
-// z = (head chunk, d chunk) folded, offset by z_base.  Block: x = vector
+// Grid: x = groups of kRowsPerThread * blockDim.z rows, y = piece (or the
+// two swapped when piece_fastest is set), z = (head chunk, d chunk) folded,
+// offset by z_base.  Block: x = vector
 // within a head row, y = head, z = row.  A thread copies one vector of each of
 // its kRowsPerThread rows: all loads first, then all stores.
 template <int VW, bool kPackedIsDst>
 __global__ void __launch_bounds__(kMaxThreads)
 relayout_rows(const __grid_constant__ Args a) {
     using V = typename Vec<VW>::T;
-    const Piece &pc = a.pieces[blockIdx.y];
+    const Piece &pc = a.pieces[a.piece_fastest ? blockIdx.x : blockIdx.y];
+    const int group = int(a.piece_fastest ? blockIdx.y : blockIdx.x);
     const int rows = int(pc.rows);
     const int rstep = int(blockDim.z);
-    const int row0 = int(blockIdx.x) * (kRowsPerThread * rstep) + int(threadIdx.z);
+    const int row0 = group * (kRowsPerThread * rstep) + int(threadIdx.z);
     const int z = int(blockIdx.z) + a.z_base;
     const int hc = z / a.dchunks;                          // block-uniform
     const int hh = hc * int(blockDim.y) + int(threadIdx.y);

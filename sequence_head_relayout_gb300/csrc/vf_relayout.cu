@@ -30,6 +30,7 @@ namespace {
 constexpr int kTargetThreads = VF_TARGET_THREADS;   // block size aimed at when rows are short
 constexpr int64_t kMaxTablePieces = int64_t(1) << 20;   // P * C limit
 constexpr int64_t kMaxGridZ = 65535;
+constexpr int64_t kMaxGridY = 65535;
 constexpr int64_t kMaxTokens = int64_t(1) << 30;
 
 // ---------------------------------------------------------------- checked math
@@ -203,6 +204,7 @@ struct Plan {
     uint16_t *packed;
     int64_t row_stride, head_stride, d_stride;
     int64_t heads, D;
+    bool piece_fastest;            // schedule the pieces of a row group together
     std::vector<vf::Piece> pieces;
 };
 
@@ -240,8 +242,11 @@ int launch_family(const Plan &pl, cudaStream_t stream) {
         for (int64_t z0 = 0; z0 < zcount; z0 += kMaxGridZ) {
             a.z_base = int32_t(z0);
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(unsigned(ceil_div(max_rows, rows_per_block)), unsigned(cnt),
-                               unsigned(std::min<int64_t>(kMaxGridZ, zcount - z0)));
+            const int64_t groups = ceil_div(max_rows, rows_per_block);
+            const unsigned zdim = unsigned(std::min<int64_t>(kMaxGridZ, zcount - z0));
+            a.piece_fastest = pl.piece_fastest && groups <= kMaxGridY;
+            cfg.gridDim = a.piece_fastest ? dim3(unsigned(cnt), unsigned(groups), zdim)
+                                          : dim3(unsigned(groups), unsigned(cnt), zdim);
             cfg.blockDim = dim3(unsigned(bx), unsigned(by), unsigned(bz));
             cfg.dynamicSmemBytes = 0;
             cfg.stream = stream;
@@ -343,6 +348,14 @@ int run(Request rq, cudaStream_t stream) {
     pl.heads = heads_per_row(s);
     pl.D = s.D;
     if (pl.heads > INT32_MAX || pl.D > INT32_MAX) return VF_ERR_ARG;
+    // The pack cuts every source token row into 3*P runs (one per slab and
+    // destination); scheduling the pieces of a row group back to back reads
+    // each source row in one burst, measured 1-3% faster on GB300.  The
+    // other ops were 2% slower that way, so they walk rows first.
+#ifndef VF_PACK_PIECE_FASTEST
+#define VF_PACK_PIECE_FASTEST 1
+#endif
+    pl.piece_fastest = VF_PACK_PIECE_FASTEST && s.op == VF_OP_QKV_PACK;
 
     // Pieces of the requested chunks, one per (c, p, slab).  Pack and merge
     // address head group p of a full-head view; the split and the unpack
