@@ -15,7 +15,7 @@ DEV = torch.device("cuda:0")
 
 
 def test_threads_on_separate_streams():
-    shapes = [(1001 + 37 * i, 8, 64, 2 + (i % 3) * 2, 1 + i % 4) for i in range(8)]
+    shapes = [(1001 + 37 * i, 8, 64, (2, 4, 8)[i % 3], 1 + i % 4) for i in range(8)]
     jobs = []
     for i, (T, H, D, P, C) in enumerate(shapes):
         g = torch.Generator().manual_seed(i)
