@@ -17,12 +17,14 @@
  * (the merge).
  *
  * The pages give no index formula; this library fixes one reading:
- *   Hp = H / P heads per destination slot (H % P == 0 for pack and merge).
+ *   Hp = H / P heads per destination slot (H % P == 0 for the pack, the
+ *   merge and the unpack).
  *   Chunk partition of n tokens into C overlap chunks: quota Q(n) =
  *   ceil(n / C); chunk c covers tokens [min(n, c*Q), min(n, (c+1)*Q)), so the
  *   last non-empty chunk may be short and trailing chunks may be empty.
  *   Packed storage is chunk blocks in order, each destination-major: block
  *   (c, p) for c = 0..C-1 (outer), p = 0..P-1 (inner), no gaps, no padding.
+ *   vf_relayout can also place the same blocks p outer (vf_order).
  *
  * Elements are 16-bit (BF16) and are moved as raw bit patterns: NaN payloads,
  * -0 and denormals arrive unchanged.  Strides are in ELEMENTS, int64, and
@@ -59,16 +61,18 @@ typedef struct CUstream_st *vf_stream_t;
 typedef enum vf_status {
     VF_OK = 0,
     /* NULL pointer with a non-empty tensor, negative dimension or stride,
-     * P < 1, C < 1, P * C > 2^20, H % P != 0 (pack, merge), T > 2^30,
-     * NULL strides for the pack or the split, a pointer that is not 2-byte
-     * aligned, a merge destination view that overlaps itself, an unknown op,
-     * or a pointer the current device cannot access (pageable host memory
-     * unknown to CUDA, another GPU's memory). */
+     * P < 1, C < 1, P * C > 2^20, H % P != 0 (pack, merge, unpack),
+     * T > 2^30, NULL strides for the pack or the split, a chunk range outside
+     * [0, C], a pointer that is not 2-byte aligned, a written view that
+     * overlaps itself, an unknown op or order, or a pointer the current
+     * device cannot access (pageable host memory unknown to CUDA, another
+     * GPU's memory). */
     VF_ERR_ARG = -1,
     /* An element count, offset or byte extent does not fit in int64. */
     VF_ERR_OVERFLOW = -2,
     /* The destination's byte range overlaps the bytes the source view
-     * addresses (the relayouts are not in-place). */
+     * addresses (the relayouts are not in-place), or two written views
+     * overlap each other (unpack). */
     VF_ERR_ALIAS = -3,
     /* The CUDA runtime reported an error while querying a pointer or
      * enqueueing a kernel (cudaGetLastError after the launch). */
@@ -96,9 +100,9 @@ typedef enum vf_order {
 
 /*
  * QKV destination pack.  ("Sol-Engine alignment on SM86 and SM89", "What is
- * enabled": QKV destination pack; the source is the merged QKV projection's
- * output, "one wide GEMM before splitting views", table "Upstream gap and
- * disposition", row "Merged QKV projection".)
+ * enabled": QKV destination pack.  The source is the output of the merged
+ * QKV projection, a single wide GEMM whose result is viewed as q, k and v:
+ * table "Upstream gap and disposition", row "Merged QKV projection".)
  *
  * src:         16-bit elements of a logical [T][3][H][D] view (token, q/k/v,
  *              head, d); src_strides[4] = its element strides in that order.
