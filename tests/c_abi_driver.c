@@ -53,6 +53,50 @@ int main(void) {
                 CHECK(h_out[t * H * D + x] == h_src[t * 3 * H * D + s * H * D + x]);
     }
 
+    /* the descriptor entry: P = 2 destinations in both block orders; the
+     * slot-major buffer must hold the chunk-major blocks at the offsets the
+     * two piece tables give */
+    {
+        const int64_t P2 = 2;
+        void *d_cm = NULL, *d_sm = NULL;
+        CHECK(cudaMalloc(&d_cm, n * 2) == cudaSuccess);
+        CHECK(cudaMalloc(&d_sm, n * 2) == cudaSuccess);
+        vf_relayout_desc desc;
+        memset(&desc, 0, sizeof(desc));
+        desc.op = VF_OP_QKV_PACK;
+        desc.T = T; desc.H = H; desc.D = D; desc.P = P2; desc.C = C;
+        desc.c_begin = 0; desc.c_count = C;
+        for (int s = 0; s < 3; ++s) desc.strided[s] = (char *)d_src + 2 * s * H * D;
+        desc.strides[0] = 3 * H * D; desc.strides[1] = D; desc.strides[2] = 1;
+        desc.order = VF_ORDER_CHUNK_MAJOR;
+        desc.packed = d_cm;
+        CHECK(vf_relayout(&desc, NULL) == VF_OK);
+        desc.order = VF_ORDER_SLOT_MAJOR;
+        desc.packed = d_sm;
+        CHECK(vf_relayout(&desc, NULL) == VF_OK);
+        desc.order = 7;
+        CHECK(vf_relayout(&desc, NULL) == VF_ERR_ARG);
+        CHECK(cudaDeviceSynchronize() == cudaSuccess);
+
+        uint16_t *h_cm = malloc(n * 2), *h_sm = malloc(n * 2);
+        CHECK(h_cm && h_sm);
+        CHECK(cudaMemcpy(h_cm, d_cm, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
+        CHECK(cudaMemcpy(h_sm, d_sm, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
+        int64_t ts[8], tl[8], off_cm[8], off_sm[8];
+        CHECK(vf_piece_table_ex(VF_OP_QKV_PACK, VF_ORDER_CHUNK_MAJOR, T, H, D, P2, C,
+                                ts, tl, off_cm, 8) == P2 * C);
+        CHECK(vf_piece_table_ex(VF_OP_QKV_PACK, VF_ORDER_SLOT_MAJOR, T, H, D, P2, C,
+                                ts, tl, off_sm, 8) == P2 * C);
+        for (int64_t e = 0; e < P2 * C; ++e) {
+            const int64_t len = tl[e] * 3 * (H / P2) * D;
+            CHECK(memcmp(h_cm + off_cm[e], h_sm + off_sm[e], len * 2) == 0);
+        }
+        free(h_cm);
+        free(h_sm);
+        cudaFree(d_cm);
+        cudaFree(d_sm);
+    }
+
     /* rejected before any launch: H % P != 0 */
     CHECK(vf_qkv_pack(d_src, st, T, H, D, 4, C, d_packed, NULL) == VF_ERR_ARG);
     CHECK(strlen(vf_status_string(VF_ERR_ARG)) > 0);
