@@ -89,86 +89,88 @@ def alg_bytes(elems: int) -> int:
 # CPU oracle (reported baseline and reference arm); runs in spawned workers
 # ----------------------------------------------------------------------------
 
-def _oracle_worker(job):
-    """One worker: run the C oracle over a token sample of the workload
-    `reps` times; return (seconds, bytes)."""
+def _oracle_inputs(T, H, D, pad, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    return {
+        "pack_src": rng.integers(0, 1 << 16, size=T * (3 * H * D + pad), dtype=np.uint16),
+        "split_src": rng.integers(0, 1 << 16, size=T * H * D, dtype=np.uint16),  # [H][T][D]
+        "merge_src": rng.integers(0, 1 << 16, size=T * H * D, dtype=np.uint16),
+        "pack_dst": np.empty(3 * T * H * D, dtype=np.uint16),
+        "split_dst": np.empty(T * H * D, dtype=np.uint16),
+        "merge_dst": np.empty(T * H * D, dtype=np.uint16),
+    }
+
+
+def _oracle_proc(rank, shape, passes, barrier, results):
+    """One host core: build a token sample of the workload once, then run the
+    C oracle's pack, split and merge over it `passes` times, each pass
+    started together with the other processes (barrier) and timed alone."""
     import ctypes
 
-    import numpy as np
-
     from oracle import build
-    T, H, D, P, C, pad, reps, seed = job
+    T, H, D, P, C, pad = shape
     lib = ctypes.CDLL(build.LIB)
     I64 = ctypes.c_int64
-    rng = np.random.default_rng(seed)
-    row = 3 * H * D + pad
-    pack_src = rng.integers(0, 1 << 16, size=T * row, dtype=np.uint16)
-    split_src = rng.integers(0, 1 << 16, size=T * H * D, dtype=np.uint16)   # [H][T][D]
-    merge_src = rng.integers(0, 1 << 16, size=T * H * D, dtype=np.uint16)
-    pack_dst = np.empty(3 * T * H * D, dtype=np.uint16)
-    split_dst = np.empty(T * H * D, dtype=np.uint16)
-    merge_dst = np.empty(T * H * D, dtype=np.uint16)
-    ps = (I64 * 4)(row, H * D, D, 1)
+    x = _oracle_inputs(T, H, D, pad, 1000 + rank)
+    ptr = {k: ctypes.c_void_p(v.ctypes.data) for k, v in x.items()}
+    ps = (I64 * 4)(3 * H * D + pad, H * D, D, 1)
     ss = (I64 * 3)(D, T * D, 1)
     ms = (I64 * 3)(H * D, D, 1)
-    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)
+    dims = (I64(T), I64(H), I64(D), I64(P), I64(C))
     for f in (lib.oracle_qkv_pack, lib.oracle_attn_split, lib.oracle_head_merge):
         f.restype = I64
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        lib.oracle_qkv_pack(ptr(pack_src), ps, I64(T), I64(H), I64(D), I64(P), I64(C), ptr(pack_dst))
-        lib.oracle_attn_split(ptr(split_src), ss, I64(T), I64(H), I64(D), I64(P), I64(C),
-                              ptr(split_dst))
-        lib.oracle_head_merge(ptr(merge_src), I64(T), I64(H), I64(D), I64(P), I64(C),
-                              ptr(merge_dst), ms)
-    dt = time.perf_counter() - t0
-    return dt, reps * alg_bytes(5 * T * H * D)
-
-
-class OraclePool:
-    """A spawn-started process pool (safe to create before or after CUDA)."""
-
-    def __init__(self, cores: int):
-        from oracle import build
-        build.build()
-        self.cores = cores
-        self.pool = mp.get_context("spawn").Pool(cores)
-
-    def run(self, cfg, tokens: int, reps: int, seed: int = 0):
-        jobs = [(tokens, cfg.H, cfg.D, cfg.P, cfg.C, cfg.pad, reps, seed + i)
-                for i in range(self.cores)]
+    times = []
+    for _ in range(passes):
+        barrier.wait()
         t0 = time.perf_counter()
-        res = self.pool.map(_oracle_worker, jobs)
-        wall = time.perf_counter() - t0
-        return wall, sum(b for _, b in res), max(t for t, _ in res)
-
-    def close(self):
-        self.pool.close()
-        self.pool.join()
+        lib.oracle_qkv_pack(ptr["pack_src"], ps, *dims, ptr["pack_dst"])
+        lib.oracle_attn_split(ptr["split_src"], ss, *dims, ptr["split_dst"])
+        lib.oracle_head_merge(ptr["merge_src"], *dims, ptr["merge_dst"], ms)
+        times.append(time.perf_counter() - t0)
+    results.put((rank, times))
 
 
-def calibrate_tokens(pool: OraclePool, cfg, seconds_per_step: float) -> int:
-    """Token count whose oracle pass takes about `seconds_per_step` per worker."""
-    probe = 256
-    _, _, t = pool.run(cfg, probe, 1)
-    per_token = max(t / probe, 1e-9)
-    return int(max(16, min(cfg.T, seconds_per_step / per_token)))
+def run_oracle(cfg, tokens: int, passes: int, cores: int):
+    """Per-pass times (the slowest core's) of `cores` processes, each moving
+    its own `tokens`-token sample; and the bytes all cores move per pass."""
+    from oracle import build
+    build.build()
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(cores)
+    results = ctx.Queue()
+    shape = (tokens, cfg.H, cfg.D, cfg.P, cfg.C, cfg.pad)
+    procs = [ctx.Process(target=_oracle_proc, args=(r, shape, passes, barrier, results))
+             for r in range(cores)]
+    for pr in procs:
+        pr.start()
+    got = [results.get() for _ in procs]
+    for pr in procs:
+        pr.join()
+    per_pass = [max(t[i] for _, t in got) for i in range(passes)]
+    return per_pass, cores * alg_bytes(5 * tokens * cfg.H * cfg.D)
+
+
+def calibrate_tokens(cfg, seconds_per_pass: float) -> int:
+    """Token count whose oracle pass takes about `seconds_per_pass` on a core."""
+    probe = min(cfg.T, 2048)
+    times, _ = run_oracle(cfg, probe, 2, 1)
+    per_token = max(min(times) / probe, 1e-9)
+    return int(max(16, min(cfg.T, seconds_per_pass / per_token)))
 
 
 def cpu_baseline(cfg, budget_s: float = 10.0, cores: int = None):
+    """The oracle on all host cores, ~budget_s of wall time in 3 passes."""
     cores = cores or os.cpu_count() or 1
-    pool = OraclePool(cores)
-    try:
-        tokens = calibrate_tokens(pool, cfg, budget_s / 3)
-        wall, nbytes, _ = pool.run(cfg, tokens, 3, seed=100)
-    finally:
-        pool.close()
-    return {"value": round(nbytes / wall / 1e9, 3), "unit": UNIT, "cores": cores,
+    tokens = calibrate_tokens(cfg, budget_s / 3)
+    per_pass, nbytes = run_oracle(cfg, tokens, 3, cores)
+    total = sum(per_pass)
+    return {"value": round(3 * nbytes / total / 1e9, 3), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": "%d of %d tokens (H=%d, D=%d, P=%d, C=%d, padded-row pack source, "
-                      "head-major split source), one independent sample per core, 3 passes "
-                      "of pack+split+merge, %.1f s wall" % (tokens, cfg.T, cfg.H, cfg.D, cfg.P,
-                                                             cfg.C, wall)}
+                      "head-major split source) per core, one process per core, 3 timed "
+                      "passes of pack+split+merge started together, %.1f s"
+                      % (tokens, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, total)}
 
 
 # ----------------------------------------------------------------------------
@@ -793,29 +795,24 @@ def per_config(args, dev):
 # ----------------------------------------------------------------------------
 
 def reference_arm(args, world):
+    """The CPU oracle on the host cores: W warm-up and K timed passes over a
+    token sample per core, sized so the whole run takes a few minutes."""
     from sequence_head_relayout_gb300 import workloads as W
     cfg = W.CONFIGS[args.config]
     cores = args.cpu_cores or os.cpu_count() or 1
-    pool = OraclePool(cores)
-    try:
-        budget = max(0.02, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-        tokens = calibrate_tokens(pool, cfg, budget)
-        for _ in range(args.warmup):
-            pool.run(cfg, tokens, 1)
-        total_wall, total_bytes = 0.0, 0
-        for i in range(args.steps):
-            wall, nbytes, _ = pool.run(cfg, tokens, 1, seed=i)
-            total_wall += wall
-            total_bytes += nbytes
-    finally:
-        pool.close()
-    value = total_bytes / total_wall / 1e9
-    sample = ("%d of %d tokens per core per step (H=%d, D=%d, P=%d, C=%d), pack+split+merge"
-              % (tokens, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C))
+    budget = max(0.02, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    tokens = calibrate_tokens(cfg, budget)
+    per_pass, nbytes = run_oracle(cfg, tokens, args.warmup + args.steps, cores)
+    timed = per_pass[args.warmup:]
+    total = sum(timed)
+    value = nbytes * len(timed) / total / 1e9
+    sample = ("%d of %d tokens per core per step (H=%d, D=%d, P=%d, C=%d), pack+split+merge, "
+              "one process per core, steps started together" % (tokens, cfg.T, cfg.H, cfg.D,
+                                                                cfg.P, cfg.C))
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total_wall / max(1, args.steps) * 1e3, 3),
+        "ms_per_step": round(total / max(1, len(timed)) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded uniform 16-bit patterns)",
         "config": {"workload": "%s: T=%d H=%d D=%d P=%d C=%d" % (cfg.name, cfg.T, cfg.H, cfg.D,
