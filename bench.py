@@ -151,12 +151,18 @@ def run_oracle(cfg, tokens: int, passes: int, cores: int):
     return per_pass, cores * alg_bytes(5 * tokens * cfg.H * cfg.D)
 
 
+SAMPLE_BYTES_PER_CORE = 1 << 30        # host memory one oracle process may hold
+
+
 def calibrate_tokens(cfg, seconds_per_pass: float) -> int:
-    """Token count whose oracle pass takes about `seconds_per_pass` on a core."""
+    """Token count whose oracle pass takes about `seconds_per_pass` on a core,
+    within SAMPLE_BYTES_PER_CORE of inputs and outputs."""
     probe = min(cfg.T, 2048)
     times, _ = run_oracle(cfg, probe, 2, 1)
     per_token = max(min(times) / probe, 1e-9)
-    return int(max(16, min(cfg.T, seconds_per_pass / per_token)))
+    bytes_per_token = 2 * ((3 * cfg.H * cfg.D + cfg.pad) + 5 * cfg.H * cfg.D + 2 * cfg.H * cfg.D)
+    cap = max(16, SAMPLE_BYTES_PER_CORE // bytes_per_token)
+    return int(max(16, min(cfg.T, cap, seconds_per_pass / per_token)))
 
 
 def cpu_baseline(cfg, budget_s: float = 10.0, cores: int = None):
