@@ -154,29 +154,32 @@ def run_oracle(cfg, tokens: int, passes: int, cores: int):
 SAMPLE_BYTES_PER_CORE = 1 << 30        # host memory one oracle process may hold
 
 
-def calibrate_tokens(cfg, seconds_per_pass: float) -> int:
+def calibrate_tokens(cfg, seconds_per_pass: float):
     """Token count whose oracle pass takes about `seconds_per_pass` on a core,
-    within SAMPLE_BYTES_PER_CORE of inputs and outputs."""
+    within SAMPLE_BYTES_PER_CORE of inputs and outputs; and the estimated
+    seconds of one pass at that count."""
     probe = min(cfg.T, 2048)
     times, _ = run_oracle(cfg, probe, 2, 1)
     per_token = max(min(times) / probe, 1e-9)
     bytes_per_token = 2 * ((3 * cfg.H * cfg.D + cfg.pad) + 5 * cfg.H * cfg.D + 2 * cfg.H * cfg.D)
     cap = max(16, SAMPLE_BYTES_PER_CORE // bytes_per_token)
-    return int(max(16, min(cfg.T, cap, seconds_per_pass / per_token)))
+    tokens = int(max(16, min(cfg.T, cap, seconds_per_pass / per_token)))
+    return tokens, tokens * per_token
 
 
 def cpu_baseline(cfg, budget_s: float = 10.0, cores: int = None):
-    """The oracle on all host cores, ~budget_s of wall time in 3 passes."""
+    """The oracle on all host cores for about budget_s of wall time."""
     cores = cores or os.cpu_count() or 1
-    tokens = calibrate_tokens(cfg, budget_s / 3)
-    per_pass, nbytes = run_oracle(cfg, tokens, 3, cores)
+    tokens, est = calibrate_tokens(cfg, budget_s / 3)
+    passes = int(max(3, min(30, budget_s / max(est, 1e-3))))
+    per_pass, nbytes = run_oracle(cfg, tokens, passes, cores)
     total = sum(per_pass)
-    return {"value": round(3 * nbytes / total / 1e9, 3), "unit": UNIT, "cores": cores,
+    return {"value": round(passes * nbytes / total / 1e9, 3), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": "%d of %d tokens (H=%d, D=%d, P=%d, C=%d, padded-row pack source, "
-                      "head-major split source) per core, one process per core, 3 timed "
+                      "head-major split source) per core, one process per core, %d timed "
                       "passes of pack+split+merge started together, %.1f s"
-                      % (tokens, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, total)}
+                      % (tokens, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, passes, total)}
 
 
 # ----------------------------------------------------------------------------
@@ -807,7 +810,7 @@ def reference_arm(args, world):
     cfg = W.CONFIGS[args.config]
     cores = args.cpu_cores or os.cpu_count() or 1
     budget = max(0.02, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    tokens = calibrate_tokens(cfg, budget)
+    tokens, _ = calibrate_tokens(cfg, budget)
     per_pass, nbytes = run_oracle(cfg, tokens, args.warmup + args.steps, cores)
     timed = per_pass[args.warmup:]
     total = sum(timed)
