@@ -330,6 +330,24 @@ def run_step(vf, cfg, s, events=None):
             events[k].record()
 
 
+def split_per_chunk_calls(vf, cfg, s, reps=50):
+    """Median time of one attention-result split call per overlap chunk (each
+    its own launch, as the pages timed the split), per chunk index."""
+    import torch
+    ts = [[] for _ in range(cfg.C)]
+    for rep in range(reps + 3):
+        for c in range(cfg.C):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            vf.attn_split(s["split_src"], cfg.P, cfg.C, out=s["split_dst"], chunks=(c, 1))
+            b.record()
+            if rep >= 3:
+                ts[c].append((a, b))
+    torch.cuda.synchronize()
+    return [round(statistics.median(x.elapsed_time(y) for x, y in t) * 1e3, 2) for t in ts]
+
+
 def launches_per_step(cfg, ops) -> int:
     """Kernel launches of one step: one per 128 pieces; a piece is one (chunk,
     destination) block, times the q/k/v slabs for the pack and the unpack."""
@@ -406,7 +424,7 @@ def gpu_arm(args, rank, world, local_rank):
                      "gbs": round(b / (med / 1e3) / 1e9, 1),
                      "frac_of_peak": round(b / (med / 1e3) / 1e9 / peak, 4)}
     if "attn_split" in ops:
-        ops["attn_split"]["per_chunk_us"] = round(ops["attn_split"]["median_us"] / cfg.C, 2)
+        ops["attn_split"]["per_chunk_call_us"] = split_per_chunk_calls(vf, cfg, sets[0])
 
     dominant = max(per_op_ms, key=lambda k: sum(per_op_ms[k]))
     avg_s = statistics.fmean(per_op_ms[dominant]) / 1e3
