@@ -250,6 +250,13 @@ int launch_family(const Plan &pl, cudaStream_t stream) {
             cfg.blockDim = dim3(unsigned(bx), unsigned(by), unsigned(bz));
             cfg.dynamicSmemBytes = 0;
             cfg.stream = stream;
+#if VF_PDL
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+#endif
             if (cudaLaunchKernelEx(&cfg, vf::relayout_rows<VW, kPackedIsDst>, a) != cudaSuccess) {
                 cudaGetLastError();
                 return VF_ERR_CUDA;
