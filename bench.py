@@ -331,21 +331,22 @@ def run_step(vf, cfg, s, events=None):
 
 
 def split_per_chunk_calls(vf, cfg, s, reps=50):
-    """Median time of one attention-result split call per overlap chunk (each
-    its own launch, as the pages timed the split), per chunk index."""
+    """The attention-result split issued as one call per overlap chunk (as
+    the pages timed it, and as an overlap pipeline issues it): the median of
+    C back-to-back chunk calls, divided by C, in microseconds."""
     import torch
-    ts = [[] for _ in range(cfg.C)]
+    ts = []
     for rep in range(reps + 3):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
         for c in range(cfg.C):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
             vf.attn_split(s["split_src"], cfg.P, cfg.C, out=s["split_dst"], chunks=(c, 1))
-            b.record()
-            if rep >= 3:
-                ts[c].append((a, b))
+        b.record()
+        if rep >= 3:
+            ts.append((a, b))
     torch.cuda.synchronize()
-    return [round(statistics.median(x.elapsed_time(y) for x, y in t) * 1e3, 2) for t in ts]
+    return round(statistics.median(x.elapsed_time(y) for x, y in ts) * 1e3 / cfg.C, 2)
 
 
 def launches_per_step(cfg, ops) -> int:
