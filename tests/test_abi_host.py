@@ -236,3 +236,28 @@ def test_relayout_descriptor_rejections(L):
     assert L.vf_relayout(ctypes.byref(d), None) == -3            # outputs alias
     assert L.vf_piece_table_ex(0, 5, 4, 4, 8, 2, 2, _i64(0, 0, 0, 0), _i64(0, 0, 0, 0),
                                _i64(0, 0, 0, 0), 4) == -1
+
+
+def test_piece_tables_random_shapes_against_oracle(L):
+    """300 random shapes, every op, both block orders: the library's host
+    tables equal the oracle's (chunk-major) and its permutation (slot-major)."""
+    import random
+    rng = random.Random(1234)
+    for _ in range(300):
+        P = rng.choice([1, 2, 3, 4, 7, 8, 16])
+        C = rng.choice([1, 2, 3, 4, 5, 9, 16])
+        H = P * rng.choice([1, 2, 3])
+        D = rng.choice([1, 8, 64, 128])
+        T = rng.choice([0, 1, 2, 5, rng.randrange(1, 200), rng.randrange(1000, 100000)])
+        for op in (0, 1, 2, 3):
+            tok, length, off = loops.piece_table(op, T, H, D, P, C)
+            assert vf.piece_table(op, T, H, D, P, C) == (tok, length, off)
+            per = {0: 3 * (H // P) * D, 1: H * D, 2: (H // P) * D, 3: 3 * (H // P) * D}[op]
+            want, cur = [0] * (P * C), 0
+            for p in range(P):
+                for c in range(C):
+                    want[c * P + p] = cur
+                    cur += length[c * P + p] * per
+            assert vf.piece_table(op, T, H, D, P, C, order="slot_major")[2] == want
+            # lengths cover every token exactly once
+            assert sum(length) == T
