@@ -259,5 +259,6 @@ def test_piece_tables_random_shapes_against_oracle(L):
                     want[c * P + p] = cur
                     cur += length[c * P + p] * per
             assert vf.piece_table(op, T, H, D, P, C, order="slot_major")[2] == want
-            # lengths cover every token exactly once
-            assert sum(length) == T
+            # every token appears once per destination slot (pack, merge: all
+            # slots see every token) or once in all (split, unpack: shards)
+            assert sum(length) == (T * P if op in (0, 2) else T)
