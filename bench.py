@@ -41,8 +41,9 @@ METRIC = "effective HBM GB/s (read+write) and % of GB300 peak per relayout op"
 UNIT = "GB/s"
 WORKLOAD = "pages"
 FALLBACK_HBM_GBS = 6800.0
+# what the GPU executes: the kernel and its launch policy (not the ABI's checks)
 KERNEL_SOURCES = ["sequence_head_relayout_gb300/csrc/relayout_kernel.cuh",
-                  "sequence_head_relayout_gb300/csrc/vf_relayout.cu"]
+                  "sequence_head_relayout_gb300/csrc/launch.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic_pages.txt")
 
 

@@ -62,7 +62,7 @@ typedef enum vf_status {
     VF_OK = 0,
     /* NULL pointer with a non-empty tensor, negative dimension or stride,
      * P < 1, C < 1, P * C > 2^20, H % P != 0 (pack, merge, unpack),
-     * T > 2^30, NULL strides for the pack or the split, a chunk range outside
+     * T, H or D > 2^30, NULL strides for the pack or the split, a chunk range outside
      * [0, C], a pointer that is not 2-byte aligned, a written view that
      * overlaps itself, an unknown op or order, or a pointer the current
      * device cannot access (pageable host memory unknown to CUDA, another

@@ -11,7 +11,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "vf_relayout.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "relayout_kernel.cuh"),
+DEPS = SOURCES + [os.path.join(CSRC, "relayout_kernel.cuh"), os.path.join(CSRC, "launch.cuh"),
                   os.path.join(ROOT, "include", "vf_relayout.h")]
 LIB = os.path.join(PKG, "libvf_relayout.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

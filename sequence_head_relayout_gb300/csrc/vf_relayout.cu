@@ -24,14 +24,8 @@
 
 namespace {
 
-#ifndef VF_TARGET_THREADS
-#define VF_TARGET_THREADS 512
-#endif
-constexpr int kTargetThreads = VF_TARGET_THREADS;   // block size aimed at when rows are short
 constexpr int64_t kMaxTablePieces = int64_t(1) << 20;   // P * C limit
-constexpr int64_t kMaxGridZ = 65535;
-constexpr int64_t kMaxGridY = 65535;
-constexpr int64_t kMaxTokens = int64_t(1) << 30;
+constexpr int64_t kMaxExtent = int64_t(1) << 30;        // T, H and D limit
 
 // ---------------------------------------------------------------- checked math
 bool mul_ok(int64_t a, int64_t b, int64_t *out) { return !__builtin_mul_overflow(a, b, out); }
@@ -59,7 +53,8 @@ int64_t slabs_of(int op) { return (op == VF_OP_QKV_PACK || op == VF_OP_QKV_UNPAC
 int check_shape(const Shape &s) {
     if (!is_op(s.op)) return VF_ERR_ARG;
     if (s.T < 0 || s.H < 0 || s.D < 0 || s.P < 1 || s.C < 1) return VF_ERR_ARG;
-    if (s.T > kMaxTokens) return VF_ERR_ARG;           // row indices stay in int32
+    // row, head and d indices stay well inside int32 in the kernel
+    if (s.T > kMaxExtent || s.H > kMaxExtent || s.D > kMaxExtent) return VF_ERR_ARG;
     if (s.op != VF_OP_ATTN_SPLIT && s.H % s.P != 0) return VF_ERR_ARG;
     int64_t n, pc;
     if (!mul_ok(s.T, s.H, &n) || !mul_ok(n, s.D, &n)) return VF_ERR_OVERFLOW;
@@ -199,101 +194,8 @@ struct Request {
     bool strided_written;          // merge, unpack
 };
 
-// Everything one launch family needs besides the pieces.
-struct Plan {
-    uint16_t *packed;
-    int64_t row_stride, head_stride, d_stride;
-    int64_t heads, D;
-    bool piece_fastest;            // schedule the pieces of a row group together
-    std::vector<vf::Piece> pieces;
-};
-
-template <int VW, bool kPackedIsDst>
-int launch_family(const Plan &pl, cudaStream_t stream) {
-    const int dvec = int(pl.D / VW);
-    const int bx = std::min(dvec, vf::kMaxThreads);
-    const int by = int(std::min<int64_t>(pl.heads, std::max(1, vf::kMaxThreads / bx)));
-    const int bz = std::max(1, std::min(64, kTargetThreads / (bx * by)));
-    const int64_t dchunks = ceil_div(dvec, bx);
-    const int64_t hchunks = ceil_div(pl.heads, by);
-    const int64_t zcount = hchunks * dchunks;              // <= heads * D
-    if (zcount > INT32_MAX) return VF_ERR_ARG;
-
-    vf::Args a;
-    std::memset(&a, 0, sizeof(a));
-    a.packed = pl.packed;
-    a.row_stride = pl.row_stride;
-    a.head_stride = pl.head_stride;
-    a.d_stride = pl.d_stride;
-    a.heads = int32_t(pl.heads);
-    a.D = int32_t(pl.D);
-    a.dchunks = int32_t(dchunks);
-
-    const int64_t rows_per_block = int64_t(vf::kRowsPerThread) * bz;
-    const size_t n = pl.pieces.size();
-    for (size_t first = 0; first < n; first += vf::kMaxPieces) {
-        const size_t cnt = std::min<size_t>(vf::kMaxPieces, n - first);
-        int64_t max_rows = 0;
-        for (size_t i = 0; i < cnt; ++i) {
-            a.pieces[i] = pl.pieces[first + i];
-            max_rows = std::max(max_rows, a.pieces[i].rows);
-        }
-        if (max_rows == 0) continue;
-        for (int64_t z0 = 0; z0 < zcount; z0 += kMaxGridZ) {
-            a.z_base = int32_t(z0);
-            cudaLaunchConfig_t cfg = {};
-            const int64_t groups = ceil_div(max_rows, rows_per_block);
-            const unsigned zdim = unsigned(std::min<int64_t>(kMaxGridZ, zcount - z0));
-            a.piece_fastest = pl.piece_fastest && groups <= kMaxGridY;
-            cfg.gridDim = a.piece_fastest ? dim3(unsigned(cnt), unsigned(groups), zdim)
-                                          : dim3(unsigned(groups), unsigned(cnt), zdim);
-            cfg.blockDim = dim3(unsigned(bx), unsigned(by), unsigned(bz));
-            cfg.dynamicSmemBytes = 0;
-            cfg.stream = stream;
-#if VF_PDL
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-#endif
-            if (cudaLaunchKernelEx(&cfg, vf::relayout_rows<VW, kPackedIsDst>, a) != cudaSuccess) {
-                cudaGetLastError();
-                return VF_ERR_CUDA;
-            }
-        }
-    }
-    return VF_OK;
-}
-
-template <bool kPackedIsDst>
-int launch_dir(const Plan &pl, int vw, cudaStream_t stream) {
-    switch (vw) {
-        case 8: return launch_family<8, kPackedIsDst>(pl, stream);
-        case 4: return launch_family<4, kPackedIsDst>(pl, stream);
-        case 2: return launch_family<2, kPackedIsDst>(pl, stream);
-        default: return launch_family<1, kPackedIsDst>(pl, stream);
-    }
-}
-
-// Widest vector (in elements) that keeps every access of both sides aligned.
-int pick_vector_width(const Plan &pl) {
-    int64_t max_rows = 0;
-    for (const auto &p : pl.pieces) max_rows = std::max(max_rows, p.rows);
-    for (int vw : {8, 4, 2}) {
-        const uintptr_t bytes = uintptr_t(2 * vw);
-        if (pl.D % vw != 0) continue;
-        if (pl.d_stride != 1) continue;
-        if (reinterpret_cast<uintptr_t>(pl.packed) % bytes) continue;
-        if (max_rows > 1 && pl.row_stride % vw) continue;
-        if (pl.heads > 1 && pl.head_stride % vw) continue;
-        bool ok = true;
-        for (const auto &p : pl.pieces)
-            ok = ok && reinterpret_cast<uintptr_t>(p.strided) % bytes == 0;
-        if (ok) return vw;
-    }
-    return 1;
-}
+// Block shape, vector width, grid order and launches.
+#include "launch.cuh"
 
 int run(Request rq, cudaStream_t stream) {
     const Shape &s = rq.s;
@@ -355,14 +257,7 @@ int run(Request rq, cudaStream_t stream) {
     pl.heads = heads_per_row(s);
     pl.D = s.D;
     if (pl.heads > INT32_MAX || pl.D > INT32_MAX) return VF_ERR_ARG;
-    // The pack cuts every source token row into 3*P runs (one per slab and
-    // destination); scheduling the pieces of a row group back to back reads
-    // each source row in one burst, measured 1-3% faster on GB300.  The
-    // other ops were 2% slower that way, so they walk rows first.
-#ifndef VF_PACK_PIECE_FASTEST
-#define VF_PACK_PIECE_FASTEST 1
-#endif
-    pl.piece_fastest = VF_PACK_PIECE_FASTEST && s.op == VF_OP_QKV_PACK;
+    pl.piece_fastest = schedule_pieces_first(s.op);
 
     // Pieces of the requested chunks, one per (c, p, slab).  Pack and merge
     // address head group p of a full-head view; the split and the unpack

@@ -115,6 +115,8 @@ FAKE_SRC, FAKE_DST = 1 << 40, 1 << 41
     (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 2, 1, None), -1),       # null dst
     (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), (1 << 30) + 1, 4, 8, 2, 1, FAKE_DST), -1),  # T > 2^30
     (("vf_qkv_pack", FAKE_SRC + 1, (96, 32, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -1),   # odd address
+    (("vf_attn_split", FAKE_SRC, (8, 8, 1), 1, 2, (1 << 30) + 8, 2, 1, FAKE_DST), -1),  # D > 2^30
+    (("vf_attn_split", FAKE_SRC, (8, 8, 1), 1, (1 << 30) + 8, 1, 2, 1, FAKE_DST), -1),  # H > 2^30
     (("vf_head_merge", FAKE_SRC, None, 4, 4, 8, 2, 1, FAKE_DST + 3), -1),           # odd address
     (("vf_qkv_pack", FAKE_SRC, (96, 32, 8, 1), 4, 4, 8, 2, 1 << 21, FAKE_DST), -1),  # P*C > 2^20
     (("vf_qkv_pack", FAKE_SRC, (1 << 62, 32, 8, 1), 4, 4, 8, 2, 1, FAKE_DST), -2),  # offset overflow
