@@ -17,7 +17,7 @@ def same(a, b):
     return torch.equal(a.reshape(-1).view(torch.int16).cpu(), b.reshape(-1).view(torch.int16))
 
 
-@pytest.mark.parametrize("name", ["tiny", "4k", "pages", "ragged"])
+@pytest.mark.parametrize("name", ["tiny", "4k", "pages", "ragged", "large"])
 def test_slot_major_all_ops(name):
     cfg = W.CONFIGS[name]
     T, H, D, P, C = cfg.T, cfg.H, cfg.D, cfg.P, cfg.C
