@@ -5,7 +5,6 @@ import subprocess
 
 import pytest
 
-import sequence_head_relayout_gb300 as vf
 
 pytestmark = pytest.mark.gpu
 
