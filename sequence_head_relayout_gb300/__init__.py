@@ -127,9 +127,21 @@ def _stream(stream, device):
 
 
 def _call(fn, *args):
-    rc = getattr(lib(), fn)(*args)
+    rc = getattr(_lib or lib(), fn)(*args)
     if rc != 0:
         raise VFError(fn, rc)
+
+
+def _n_packed(op, T, H, D, P):
+    """Packed element count for sizing outputs (the library validates the
+    shape again on every call); odd shapes go through the library's check."""
+    if P < 1 or min(T, H, D) < 0:
+        return packed_elems(op, T, H, D, P, 1)            # raises VFError
+    if op == OP_QKV_PACK:
+        return 3 * T * H * D
+    if op == OP_QKV_UNPACK:
+        return 3 * T * (H // P) * D
+    return T * H * D
 
 
 def packed_elems(op: int, T: int, H: int, D: int, P: int, C: int) -> int:
@@ -142,9 +154,10 @@ def packed_elems(op: int, T: int, H: int, D: int, P: int, C: int) -> int:
 
 
 def _order(order) -> int:
-    if order not in ORDERS:
+    o = ORDERS.get(order)
+    if o is None:
         raise ValueError("order must be one of %s" % sorted(ORDERS))
-    return ORDERS[order]
+    return o
 
 
 def piece_table(op: int, T: int, H: int, D: int, P: int, C: int, order="chunk_major"):
@@ -198,7 +211,7 @@ def qkv_pack(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
     if src.dim() != 4 or src.shape[1] != 3:
         raise ValueError("src must be a [T,3,H,D] view")
     T, _, H, D = src.shape
-    out = _flat_out(out, packed_elems(OP_QKV_PACK, T, H, D, P, C), src)
+    out = _flat_out(out, _n_packed(OP_QKV_PACK, T, H, D, P), src)
     o = _order(order)
     if o:
         st = src.stride()
@@ -223,7 +236,7 @@ def qkv_pack3(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, C: int,
     if q.stride() != k.stride() or q.stride() != v.stride():
         raise ValueError("q, k, v must share their strides")
     T, H, D = q.shape
-    out = _flat_out(out, packed_elems(OP_QKV_PACK, T, H, D, P, C), q)
+    out = _flat_out(out, _n_packed(OP_QKV_PACK, T, H, D, P), q)
     o = _order(order)
     if o:
         _relayout(OP_QKV_PACK, o, T, H, D, P, C, chunks, out.data_ptr(),
@@ -248,7 +261,7 @@ def attn_split(src: torch.Tensor, P: int, C: int, out: torch.Tensor = None,
     if src.dim() != 3:
         raise ValueError("src must be a [T,H,D] view")
     T, H, D = src.shape
-    out = _flat_out(out, packed_elems(OP_ATTN_SPLIT, T, H, D, P, C), src)
+    out = _flat_out(out, _n_packed(OP_ATTN_SPLIT, T, H, D, P), src)
     o = _order(order)
     if o:
         _relayout(OP_ATTN_SPLIT, o, T, H, D, P, C, chunks, out.data_ptr(), [src.data_ptr()],
@@ -269,7 +282,7 @@ def head_merge(src: torch.Tensor, T: int, H: int, D: int, P: int, C: int,
     contiguous tensor is allocated when it is omitted.
     """
     _check16(src, "src")
-    n = packed_elems(OP_HEAD_MERGE, T, H, D, P, C)
+    n = _n_packed(OP_HEAD_MERGE, T, H, D, P)
     if not src.is_contiguous() or src.numel() != n:
         raise ValueError("src must be contiguous with %d elements" % n)
     if out is None:
@@ -298,7 +311,7 @@ def qkv_unpack(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int, outs=
     stride tuple; contiguous tensors are allocated when it is omitted.
     """
     _check16(recv, "recv")
-    n = packed_elems(OP_QKV_UNPACK, T, H, D, P, C)
+    n = _n_packed(OP_QKV_UNPACK, T, H, D, P)
     if not recv.is_contiguous() or recv.numel() != n:
         raise ValueError("recv must be contiguous with %d elements" % n)
     Hp = H // P
