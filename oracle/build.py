@@ -20,8 +20,10 @@ def build(force: bool = False) -> str:
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB + ".tmp.%d" % os.getpid()
+    # float32 arithmetic exactly as written: no contraction into fused
+    # multiply-adds, no fast-math; libm for rintf/frexpf/ldexpf
     cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra", "-Werror",
-           "-o", tmp, SRC]
+           "-ffp-contract=off", "-fno-fast-math", "-o", tmp, SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

@@ -17,6 +17,7 @@ OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE, OP_QKV_UNPACK = 0, 1, 2, 3
 _lib = None
 _I64 = ctypes.c_int64
 _P = ctypes.c_void_p
+_INT = ctypes.c_int
 
 
 def lib():
@@ -36,10 +37,21 @@ def lib():
                                    arr4, arr4, arr4, _I64],
             "oracle_reorder_blocks": [ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _P, _P,
                                       ctypes.c_int],
+            "oracle_qkv_pack_q": [_P, arr4, _I64, _I64, _I64, _I64, _I64, _INT, _P, _P],
+            "oracle_qkv_unpack_q": [_P, _P, _I64, _I64, _I64, _I64, _I64, _INT, _P, _P, _P,
+                                    arr4],
+            "oracle_attn_split_q": [_P, arr4, _I64, _I64, _I64, _I64, _I64, _INT, _P, _P],
+            "oracle_head_merge_q": [_P, _P, _I64, _I64, _I64, _I64, _I64, _INT, _P, arr4],
         }.items():
             f = getattr(l, name)
             f.argtypes = args
             f.restype = _I64
+        l.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        l.oracle_e4m3_encode.restype = ctypes.c_uint8
+        l.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        l.oracle_e4m3_decode.restype = ctypes.c_float
+        l.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        l.oracle_f32_to_bf16.restype = ctypes.c_uint16
         _lib = l
     return _lib
 
@@ -172,3 +184,70 @@ def to_chunk_major(op: int, packed: torch.Tensor, T: int, H: int, D: int, P: int
     n = lib().oracle_reorder_blocks(op, T, H, D, P, C, src.data_ptr(), out.data_ptr(), 0)
     _check(n, src.numel(), "reorder_blocks")
     return out
+
+
+# ---- lossy transport (opt-in) ---------------------------------------------
+# fmt: INT8 = 1, E4M3 = 2.  Codes are one byte per element (int8 or uint8
+# bits), scales one float32 per head row, both in the exact op's layout.
+
+INT8, E4M3 = 1, 2
+
+
+def _code_dtype(fmt):
+    return torch.int8 if fmt == INT8 else torch.uint8
+
+
+def qkv_pack_q(src: torch.Tensor, P: int, C: int, fmt: int):
+    """Quantising QKV pack of a [T,3,H,D] view -> (codes, scales)."""
+    s = _bits(src)
+    T, _, H, D = s.shape
+    codes = torch.empty(3 * T * H * D, dtype=_code_dtype(fmt))
+    scales = torch.empty(3 * T * H, dtype=torch.float32)
+    n = lib().oracle_qkv_pack_q(s.data_ptr(), _strides(s), T, H, D, P, C, fmt,
+                                codes.data_ptr(), scales.data_ptr())
+    _check(n, codes.numel(), "qkv_pack_q")
+    return codes, scales
+
+
+def attn_split_q(src: torch.Tensor, P: int, C: int, fmt: int):
+    """Quantising attention-result split of a [T,H,D] view -> (codes, scales)."""
+    s = _bits(src)
+    T, H, D = s.shape
+    codes = torch.empty(T * H * D, dtype=_code_dtype(fmt))
+    scales = torch.empty(T * H, dtype=torch.float32)
+    n = lib().oracle_attn_split_q(s.data_ptr(), _strides(s), T, H, D, P, C, fmt,
+                                  codes.data_ptr(), scales.data_ptr())
+    _check(n, codes.numel(), "attn_split_q")
+    return codes, scales
+
+
+def head_merge_q(codes, scales, T, H, D, P, C, fmt):
+    """Dequantising merge -> [T,H,D] bf16 bits (int16)."""
+    out = torch.empty((T, H, D), dtype=torch.int16)
+    n = lib().oracle_head_merge_q(codes.contiguous().data_ptr(), scales.contiguous().data_ptr(),
+                                  T, H, D, P, C, fmt, out.data_ptr(), _strides(out))
+    _check(n, T * H * D, "head_merge_q")
+    return out
+
+
+def qkv_unpack_q(codes, scales, T, H, D, P, C, fmt):
+    """Dequantising receive-side unpack -> Q, K, V as [T,H/P,D] bf16 bits."""
+    Hp = H // P
+    outs = tuple(torch.empty((T, Hp, D), dtype=torch.int16) for _ in range(3))
+    n = lib().oracle_qkv_unpack_q(codes.contiguous().data_ptr(), scales.contiguous().data_ptr(),
+                                  T, H, D, P, C, fmt, outs[0].data_ptr(), outs[1].data_ptr(),
+                                  outs[2].data_ptr(), _strides(outs[0]))
+    _check(n, 3 * T * Hp * D, "qkv_unpack_q")
+    return outs
+
+
+def e4m3_encode(x: float) -> int:
+    return int(lib().oracle_e4m3_encode(x))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(lib().oracle_e4m3_decode(c))
+
+
+def f32_to_bf16(x: float) -> int:
+    return int(lib().oracle_f32_to_bf16(x))

@@ -44,7 +44,9 @@
  * of elements its cursor moved (a negative value on bad arguments).
  * Strides are in elements.
  */
+#include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 /* ---- partitions (reading of the four-chunk overlap layout) ------------- */
 
@@ -358,3 +360,202 @@ int64_t oracle_reorder_blocks(int op, int64_t T, int64_t H, int64_t D, int64_t P
         }
     return k;
 }
+
+/* ---- lossy transport (opt-in variant) ----------------------------------- */
+
+/*
+ * "Sol-Engine alignment on SM86 and SM89", table "Upstream gap and
+ * disposition", row "INT8 QKV and FP8 output transport": a fast upstream
+ * profile moves Q/K/V as INT8 and the attention output as FP8 across the
+ * exchange; the pages keep it out of the exact default.  The pages give no
+ * format, so the reading here is the plainest symmetric one, decided in
+ * float32 exactly as written so that both sides take the same integer
+ * decisions.  fmt 1 = INT8, fmt 2 = FP8 E4M3; any op takes either format
+ * (the pages pair INT8 with the QKV pack/unpack and FP8 with the attention
+ * output's split/merge).
+ *   Per head row (the D elements of one token and one head): amax = max |x|.
+ *   A row with amax < 2^-96 (all zero, or so small that 1/amax would leave
+ *   the float range) is sent as scale 0 and all codes 0.  Otherwise, with
+ *   top = 127 (INT8) or 448 (E4M3):
+ *     inv = top / amax, scale = amax / top   (each rounded once);
+ *     q = x * inv                            (rounded once);
+ *     INT8: code = clamp(round_half_even(q), -127, 127);
+ *     E4M3 (OCP 8-bit floating point: 1 sign, 4 exponent bits with bias 7,
+ *           3 mantissa bits, no infinities, largest finite 448): code = q
+ *           rounded to the nearest E4M3 value, ties to even, |q| >= 448
+ *           saturating to +-448.
+ *   Dequantisation: y = bf16(value(code) * scale), the product rounded to
+ *   float32, then to bfloat16, both to nearest even.
+ * The 2^-96 floor keeps every intermediate a normal float32, so the codes do
+ * not depend on whether denormals are flushed.  Codes use the element layout
+ * of the exact ops (one byte per element); scales are one float per head row
+ * in the order of the rows in that layout (scale index = element offset / D).
+ * Inputs must be finite.  rintf() uses the default rounding mode (nearest,
+ * ties to even).
+ */
+
+static float bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* float32 -> bfloat16, round to nearest, ties to even (finite inputs): keep
+ * the top 16 bits after adding half of the dropped range, plus one when the
+ * kept part is odd (so that an exact half rounds to the even neighbour). */
+static uint16_t f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* E4M3 encoding of a float, nearest-even, saturating (finite inputs). */
+static uint8_t e4m3_encode(float f) {
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    float a = fabsf(f);
+    if (a >= 448.0f) return (uint8_t)(sign | 0x7E);          /* 1.75 * 2^8 */
+    if (a < 0.015625f) {                                      /* below 2^-6: subnormal grid 2^-9 */
+        int m = (int)rintf(a * 512.0f);                       /* exact scaling by 2^9 */
+        if (m >= 8) return (uint8_t)(sign | 0x08);            /* rounds up to 2^-6 */
+        return (uint8_t)(sign | m);
+    }
+    int e;
+    float fr = frexpf(a, &e);                                 /* a = fr * 2^e, fr in [0.5,1) */
+    int exp = e - 1;                                          /* a = (2 fr) * 2^exp */
+    float mant = (2.0f * fr - 1.0f) * 8.0f;                   /* exact: 3 mantissa bits */
+    int m = (int)rintf(mant);
+    if (m == 8) {
+        m = 0;
+        exp += 1;
+    }
+    if (exp > 8 || (exp == 8 && m > 6)) return (uint8_t)(sign | 0x7E);
+    return (uint8_t)(sign | ((exp + 7) << 3) | m);
+}
+
+static float e4m3_decode(uint8_t c) {
+    float sign = (c & 0x80) ? -1.0f : 1.0f;
+    int exp = (c >> 3) & 0xF, m = c & 7;
+    if (exp == 0) return sign * ldexpf((float)m, -9);
+    return sign * ldexpf(1.0f + (float)m / 8.0f, exp - 7);
+}
+
+static int bad_fmt(int fmt) { return fmt != 1 && fmt != 2; }
+
+/* Quantise one head row of D elements read at x[d * ds]. */
+static void quantise_row(const uint16_t *x, int64_t ds, int64_t D, int fmt,
+                         uint8_t *codes, float *scale) {
+    float amax = 0.0f;
+    for (int64_t d = 0; d < D; ++d) {
+        float v = fabsf(bf16_to_f32(x[d * ds]));
+        if (v > amax) amax = v;
+    }
+    const float top = fmt == 2 ? 448.0f : 127.0f;
+    const int live = amax >= 0x1p-96f;
+    const float inv = live ? top / amax : 0.0f;
+    *scale = live ? amax / top : 0.0f;
+    for (int64_t d = 0; d < D; ++d) {
+        const float q = bf16_to_f32(x[d * ds]) * inv;
+        if (!live) {
+            codes[d] = 0;
+        } else if (fmt == 2) {
+            codes[d] = e4m3_encode(q);
+        } else {
+            float r = rintf(q);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            codes[d] = (uint8_t)(int8_t)r;
+        }
+    }
+}
+
+static uint16_t dequantise(uint8_t code, float scale, int fmt) {
+    const float v = fmt == 2 ? e4m3_decode(code) : (float)(int8_t)code;
+    return f32_to_bf16(v * scale);
+}
+
+/* Quantising QKV pack: the pack's loop nest, one head row at a time. */
+int64_t oracle_qkv_pack_q(const uint16_t *src, const int64_t st[4],
+                          int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, int fmt,
+                          uint8_t *codes, float *scales) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0 || bad_fmt(fmt)) return -1;
+    const int64_t Hp = H / P;
+    int64_t k = 0, r = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        const int64_t t0 = part_begin(T, C, c), t1 = part_end(T, C, c);
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t s = 0; s < 3; ++s)
+                for (int64_t t = t0; t < t1; ++t)
+                    for (int64_t hh = 0; hh < Hp; ++hh, ++r, k += D)
+                        quantise_row(src + t * st[0] + s * st[1] + (p * Hp + hh) * st[2],
+                                     st[3], D, fmt, codes + k, scales + r);
+    }
+    return k;
+}
+
+/* Dequantising receive-side unpack: the unpack's loop nest. */
+int64_t oracle_qkv_unpack_q(const uint8_t *codes, const float *scales,
+                            int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, int fmt,
+                            uint16_t *q, uint16_t *k_out, uint16_t *v, const int64_t ot[3]) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0 || bad_fmt(fmt)) return -1;
+    const int64_t Hp = H / P;
+    uint16_t *outs[3] = {q, k_out, v};
+    int64_t k = 0, r = 0;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t rk = 0; rk < P; ++rk) {
+            const int64_t a = part_begin(T, P, rk);
+            const int64_t n = part_end(T, P, rk) - a;
+            const int64_t u0 = part_begin(n, C, c), u1 = part_end(n, C, c);
+            for (int64_t s = 0; s < 3; ++s)
+                for (int64_t u = u0; u < u1; ++u)
+                    for (int64_t hh = 0; hh < Hp; ++hh, ++r)
+                        for (int64_t d = 0; d < D; ++d, ++k)
+                            outs[s][(a + u) * ot[0] + hh * ot[1] + d * ot[2]] =
+                                dequantise(codes[k], scales[r], fmt);
+        }
+    return k;
+}
+
+/* Quantising attention-result split: the split's loop nest. */
+int64_t oracle_attn_split_q(const uint16_t *src, const int64_t st[3],
+                            int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, int fmt,
+                            uint8_t *codes, float *scales) {
+    if (bad_dims(T, H, D, P, C) || bad_fmt(fmt)) return -1;
+    int64_t k = 0, r = 0;
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t p = 0; p < P; ++p) {
+            const int64_t a = part_begin(T, P, p);
+            const int64_t n = part_end(T, P, p) - a;
+            const int64_t u0 = part_begin(n, C, c), u1 = part_end(n, C, c);
+            for (int64_t u = u0; u < u1; ++u)
+                for (int64_t h = 0; h < H; ++h, ++r, k += D)
+                    quantise_row(src + (a + u) * st[0] + h * st[1], st[2], D, fmt,
+                                 codes + k, scales + r);
+        }
+    return k;
+}
+
+/* Dequantising returned-head merge: the merge's loop nest. */
+int64_t oracle_head_merge_q(const uint8_t *codes, const float *scales,
+                            int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, int fmt,
+                            uint16_t *dst, const int64_t dt[3]) {
+    if (bad_dims(T, H, D, P, C) || H % P != 0 || bad_fmt(fmt)) return -1;
+    const int64_t Hp = H / P;
+    int64_t k = 0, r = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        const int64_t t0 = part_begin(T, C, c), t1 = part_end(T, C, c);
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t t = t0; t < t1; ++t)
+                for (int64_t hh = 0; hh < Hp; ++hh, ++r)
+                    for (int64_t d = 0; d < D; ++d, ++k)
+                        dst[t * dt[0] + (p * Hp + hh) * dt[1] + d * dt[2]] =
+                            dequantise(codes[k], scales[r], fmt);
+    }
+    return k;
+}
+
+/* Exposed for the pins: the scalar conversions used above. */
+uint8_t oracle_e4m3_encode(float f) { return e4m3_encode(f); }
+float oracle_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
+uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16(f); }
