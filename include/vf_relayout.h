@@ -275,6 +275,69 @@ int64_t vf_piece_table_ex(int op, int order, int64_t T, int64_t H, int64_t D, in
                           int64_t C, int64_t *tok_start, int64_t *tok_len,
                           int64_t *packed_off, int64_t cap);
 
+/*
+ * Opt-in lossy transport.  ("Sol-Engine alignment on SM86 and SM89", table
+ * "Upstream gap and disposition", row "INT8 QKV and FP8 output transport": a
+ * profile that moves Q/K/V as INT8 and the attention output as FP8 across the
+ * exchange.  The pages keep it out of the exact default and give no format;
+ * nothing above changes when these calls are not used.)
+ *
+ * Format, per head row (the D elements of one token and one head), all in
+ * float32 with one rounding per step, to nearest even:
+ *   amax = max |x|.  If amax < 2^-96: scale = 0 and every code is 0.
+ *   Else, top = 127 (VF_FORMAT_INT8) or 448 (VF_FORMAT_E4M3):
+ *     inv = top / amax;  scale = amax / top;  q = x * inv;
+ *     INT8: code = clamp(round(q), -127, 127), an int8 byte;
+ *     E4M3: code = q as OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7,
+ *           3 mantissa bits), saturating at +-448, never NaN.
+ *   Receive side: y = bfloat16(value(code) * scale).
+ * Inputs must be finite (NaN or infinity gives unspecified codes).
+ *
+ * Storage: codes: one byte per element, in exactly the element layout of
+ * the exact op (vf_packed_elems bytes; block offsets are vf_piece_table's
+ * packed_off in bytes).  scales: one float per head row of that layout, in
+ * the same order (vf_scale_count floats; row i covers code bytes
+ * [i*D, (i+1)*D)); 4-byte aligned.  Codes and scales must not overlap each
+ * other or the strided views.  Codes may be at any address; the kernels use
+ * 8-element vectors when D % 8 == 0, the strided side is 16-byte aligned
+ * with d contiguous, and codes are 8-byte aligned.
+ * Additional limit: tokens x heads of any one (chunk, destination) block
+ * below 2^31, else VF_ERR_ARG.
+ */
+typedef enum vf_format {
+    VF_FORMAT_INT8 = 1,
+    VF_FORMAT_E4M3 = 2
+} vf_format;
+
+/* vf_relayout with quantised packed storage: desc->packed holds the codes
+ * (written by the pack and the split, read by the merge and the unpack) and
+ * `scales` the per-row scales (written or read likewise).  Any op, order and
+ * chunk range; an unknown format is VF_ERR_ARG. */
+int vf_relayout_q(const vf_relayout_desc *desc, int format, float *scales,
+                  vf_stream_t stream);
+
+/* The pairings the pages name: INT8 for the QKV pack and its receive-side
+ * unpack, E4M3 for the attention-result split and the returned-head merge.
+ * Arguments as for the exact entry points, with the 16-bit packed buffer
+ * replaced by codes + scales. */
+int vf_qkv_pack_int8(const void *src, const int64_t src_strides[4],
+                     int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                     void *codes, float *scales, vf_stream_t stream);
+int vf_qkv_unpack_int8(const void *codes, const float *scales,
+                       int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                       void *q, void *k, void *v, const int64_t out_strides[3],
+                       vf_stream_t stream);
+int vf_attn_split_fp8(const void *src, const int64_t src_strides[3],
+                      int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                      void *codes, float *scales, vf_stream_t stream);
+int vf_head_merge_fp8(const void *codes, const float *scales, const int64_t dst_strides[3],
+                      int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
+                      void *dst, vf_stream_t stream);
+
+/* Number of scales of `op`'s packed side: vf_packed_elems / D (0 when D is
+ * 0), or a negative vf_status.  Pure host function. */
+int64_t vf_scale_count(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C);
+
 /* Static, NUL-terminated description of a vf_status value. */
 const char *vf_status_string(int status);
 

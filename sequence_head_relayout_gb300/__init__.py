@@ -23,6 +23,14 @@ Every function takes ``chunks=(c_begin, c_count)`` to move only those overlap
 chunks (the packed buffer is always the full one) and ``order`` for the block
 order of the packed storage: ``"chunk_major"`` ([c][p], the four-chunk overlap
 layout, default) or ``"slot_major"`` ([p][c]).
+
+Opt-in lossy transport (same page, table "Upstream gap and disposition", row
+"INT8 QKV and FP8 output transport"): :func:`qkv_pack_q`, :func:`attn_split_q`,
+:func:`head_merge_q` and :func:`qkv_unpack_q` quantise each head row to
+8-bit codes (``fmt="int8"`` -> int8 codes, ``fmt="e4m3"`` -> float8_e4m3fn
+codes) plus one float32 scale per head row, in the exact ops' layout, and
+dequantise to bfloat16 on the receive side.  The format is stated in
+``include/vf_relayout.h``.
 """
 import ctypes
 import os
@@ -31,10 +39,12 @@ import torch
 
 __all__ = ["qkv_pack", "qkv_pack3", "attn_split", "head_merge", "qkv_unpack", "packed_elems",
            "piece_table", "VFError", "lib", "OP_QKV_PACK", "OP_ATTN_SPLIT", "OP_HEAD_MERGE",
-           "OP_QKV_UNPACK"]
+           "OP_QKV_UNPACK", "qkv_pack_q", "attn_split_q", "head_merge_q", "qkv_unpack_q",
+           "scale_count", "FORMATS"]
 
 OP_QKV_PACK, OP_ATTN_SPLIT, OP_HEAD_MERGE, OP_QKV_UNPACK = 0, 1, 2, 3
 ORDERS = {"chunk_major": 0, "slot_major": 1}
+FORMATS = {"int8": 1, "e4m3": 2}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libvf_relayout.so")
@@ -95,6 +105,19 @@ def lib():
         l.vf_piece_table_ex.restype = _I64
         l.vf_relayout.argtypes = [ctypes.POINTER(_Desc), _P]
         l.vf_relayout.restype = ctypes.c_int
+        l.vf_relayout_q.argtypes = [ctypes.POINTER(_Desc), ctypes.c_int, _P, _P]
+        l.vf_relayout_q.restype = ctypes.c_int
+        for name, args in {
+            "vf_qkv_pack_int8": [_P, _I64P] + [_I64] * 5 + [_P, _P, _P],
+            "vf_qkv_unpack_int8": [_P, _P] + [_I64] * 5 + [_P, _P, _P, _I64P, _P],
+            "vf_attn_split_fp8": [_P, _I64P] + [_I64] * 5 + [_P, _P, _P],
+            "vf_head_merge_fp8": [_P, _P, _I64P] + [_I64] * 5 + [_P, _P],
+        }.items():
+            f = getattr(l, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        l.vf_scale_count.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, _I64]
+        l.vf_scale_count.restype = _I64
         l.vf_status_string.argtypes = [ctypes.c_int]
         l.vf_status_string.restype = ctypes.c_char_p
         _lib = l
@@ -175,8 +198,10 @@ def _range(chunks, C):
     return (0, C) if chunks is None else (int(chunks[0]), int(chunks[1]))
 
 
-def _relayout(op, order, T, H, D, P, C, chunks, packed, strided, strides, stream):
-    """vf_relayout with a descriptor (the general entry, any block order)."""
+def _relayout(op, order, T, H, D, P, C, chunks, packed, strided, strides, stream,
+              fmt=0, scales=None):
+    """vf_relayout (or vf_relayout_q with a format) with a descriptor: the
+    general entry, any block order."""
     c0, cn = _range(chunks, C)
     d = _Desc(op=op, order=order, T=T, H=H, D=D, P=P, C=C, c_begin=c0, c_count=cn,
               packed=packed)
@@ -184,6 +209,11 @@ def _relayout(op, order, T, H, D, P, C, chunks, packed, strided, strides, stream
         d.strided[i] = ptr
     for i, st in enumerate(strides):
         d.strides[i] = st
+    if fmt:
+        rc = lib().vf_relayout_q(ctypes.byref(d), fmt, scales, stream)
+        if rc != 0:
+            raise VFError("vf_relayout_q", rc)
+        return
     rc = lib().vf_relayout(ctypes.byref(d), stream)
     if rc != 0:
         raise VFError("vf_relayout", rc)
@@ -334,4 +364,131 @@ def qkv_unpack(recv: torch.Tensor, T: int, H: int, D: int, P: int, C: int, outs=
     c0, cn = _range(chunks, C)
     _call("vf_qkv_unpack_chunks", recv.data_ptr(), T, H, D, P, C, c0, cn, q.data_ptr(),
           k.data_ptr(), v.data_ptr(), _strides(q), _stream(stream, recv.device))
+    return outs
+
+
+# ---- opt-in lossy transport --------------------------------------------------
+
+def _fmt(fmt) -> int:
+    f = FORMATS.get(fmt)
+    if f is None:
+        raise ValueError("fmt must be one of %s" % sorted(FORMATS))
+    return f
+
+
+def _code_dtype(f):
+    return torch.int8 if f == 1 else torch.float8_e4m3fn
+
+
+def _gpu_addressable(t, what):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % what)
+    if t.device.type != "cuda" and not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError("%s must be a CUDA tensor or pinned host memory "
+                         "(there is no CPU path)" % what)
+
+
+def scale_count(op: int, T: int, H: int, D: int, P: int, C: int) -> int:
+    """Scales (one per head row) of the packed side of ``op``."""
+    n = lib().vf_scale_count(op, T, H, D, P, C)
+    if n < 0:
+        raise VFError("vf_scale_count", n)
+    return n
+
+
+def _codes_scales(codes, scales, n, rows, f, like, what):
+    """Check (or allocate) the flat codes and scales buffers."""
+    if codes is None:
+        codes = torch.empty(n, dtype=_code_dtype(f), device=like.device,
+                            pin_memory=like.device.type == "cpu")
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=like.device,
+                             pin_memory=like.device.type == "cpu")
+    _gpu_addressable(codes, what + " codes")
+    _gpu_addressable(scales, what + " scales")
+    if codes.element_size() != 1 or not codes.is_contiguous() or codes.numel() != n:
+        raise ValueError("codes must be a contiguous 8-bit tensor of %d elements" % n)
+    if scales.dtype != torch.float32 or not scales.is_contiguous() or scales.numel() != rows:
+        raise ValueError("scales must be a contiguous float32 tensor of %d elements" % rows)
+    return codes, scales
+
+
+def _rows(n, D):
+    return n // D if D > 0 else 0
+
+
+def qkv_pack_q(src: torch.Tensor, P: int, C: int, fmt="int8", codes=None, scales=None,
+               stream: torch.cuda.Stream = None, chunks=None, order="chunk_major"):
+    """Quantising QKV pack of a [T,3,H,D] bf16 view -> (codes, scales): the
+    layout of :func:`qkv_pack`, one byte per element, one scale per head row."""
+    _check16(src, "src")
+    if src.dim() != 4 or src.shape[1] != 3:
+        raise ValueError("src must be a [T,3,H,D] view")
+    f = _fmt(fmt)
+    T, _, H, D = src.shape
+    n = _n_packed(OP_QKV_PACK, T, H, D, P)
+    codes, scales = _codes_scales(codes, scales, n, _rows(n, D), f, src, "pack")
+    st = src.stride()
+    bases = [src.data_ptr() + s * st[1] * src.element_size() for s in range(3)]
+    _relayout(OP_QKV_PACK, _order(order), T, H, D, P, C, chunks, codes.data_ptr(), bases,
+              (st[0], st[2], st[3]), _stream(stream, src.device), f, scales.data_ptr())
+    return codes, scales
+
+
+def attn_split_q(src: torch.Tensor, P: int, C: int, fmt="e4m3", codes=None, scales=None,
+                 stream: torch.cuda.Stream = None, chunks=None, order="chunk_major"):
+    """Quantising attention-result split of a [T,H,D] bf16 view -> (codes, scales)."""
+    _check16(src, "src")
+    if src.dim() != 3:
+        raise ValueError("src must be a [T,H,D] view")
+    f = _fmt(fmt)
+    T, H, D = src.shape
+    n = _n_packed(OP_ATTN_SPLIT, T, H, D, P)
+    codes, scales = _codes_scales(codes, scales, n, _rows(n, D), f, src, "split")
+    _relayout(OP_ATTN_SPLIT, _order(order), T, H, D, P, C, chunks, codes.data_ptr(),
+              [src.data_ptr()], src.stride(), _stream(stream, src.device), f,
+              scales.data_ptr())
+    return codes, scales
+
+
+def head_merge_q(codes: torch.Tensor, scales: torch.Tensor, T: int, H: int, D: int, P: int,
+                 C: int, fmt="e4m3", out: torch.Tensor = None,
+                 stream: torch.cuda.Stream = None, chunks=None, order="chunk_major"):
+    """Dequantising returned-head merge -> [T,H,D] bfloat16 (or into ``out``)."""
+    f = _fmt(fmt)
+    n = _n_packed(OP_HEAD_MERGE, T, H, D, P)
+    codes, scales = _codes_scales(codes, scales, n, _rows(n, D), f, codes, "merge")
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=codes.device,
+                          pin_memory=codes.device.type == "cpu")
+    _check16(out, "out")
+    if tuple(out.shape) != (T, H, D):
+        raise ValueError("out must have shape [T,H,D]")
+    _relayout(OP_HEAD_MERGE, _order(order), T, H, D, P, C, chunks, codes.data_ptr(),
+              [out.data_ptr()], out.stride(), _stream(stream, codes.device), f,
+              scales.data_ptr())
+    return out
+
+
+def qkv_unpack_q(codes: torch.Tensor, scales: torch.Tensor, T: int, H: int, D: int, P: int,
+                 C: int, fmt="int8", outs=None, stream: torch.cuda.Stream = None,
+                 chunks=None, order="chunk_major"):
+    """Dequantising receive-side unpack -> (Q, K, V), each [T,H/P,D] bfloat16."""
+    f = _fmt(fmt)
+    n = _n_packed(OP_QKV_UNPACK, T, H, D, P)
+    codes, scales = _codes_scales(codes, scales, n, _rows(n, D), f, codes, "unpack")
+    Hp = H // P
+    if outs is None:
+        outs = tuple(torch.empty((T, Hp, D), dtype=torch.bfloat16, device=codes.device,
+                                 pin_memory=codes.device.type == "cpu") for _ in range(3))
+    q, k, v = outs
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _check16(t, name)
+        if tuple(t.shape) != (T, Hp, D):
+            raise ValueError("%s must have shape [T,H/P,D]" % name)
+    if q.stride() != k.stride() or q.stride() != v.stride():
+        raise ValueError("q, k, v must share their strides")
+    _relayout(OP_QKV_UNPACK, _order(order), T, H, D, P, C, chunks, codes.data_ptr(),
+              [q.data_ptr(), k.data_ptr(), v.data_ptr()], q.stride(),
+              _stream(stream, codes.device), f, scales.data_ptr())
     return outs

@@ -1,0 +1,124 @@
+// Launch policy of the lossy-transport kernels (quant_kernel.cuh): vector
+// width, head-row group size, grid and the launches.  The host checks and the
+// piece tables live in vf_relayout.cu; this file decides what the GPU
+// executes for the quantising and dequantising relayouts.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include "quant.h"
+#include "vf_relayout.h"
+
+namespace vfq {
+namespace {
+
+static_assert(vf::kFmtInt8 == VF_FORMAT_INT8 && vf::kFmtE4M3 == VF_FORMAT_E4M3,
+              "kernel format tags follow vf_format");
+
+constexpr int64_t kMaxGridX = int64_t(1) << 20;   // the kernels stride over head rows
+
+// Widest vector (elements) that keeps every access of both sides aligned:
+// codes need VW-byte alignment (row starts are multiples of D), the
+// strided side 2*VW bytes.
+int pick_vector_width(const Plan &pl) {
+    int64_t max_rows = 0;
+    for (const auto &p : pl.pieces) max_rows = std::max(max_rows, p.rows);
+    for (int vw : {8, 4, 2}) {
+        if (pl.D % vw != 0 || pl.d_stride != 1) continue;
+        if (reinterpret_cast<uintptr_t>(pl.codes) % uintptr_t(vw)) continue;
+        if (max_rows > 1 && pl.row_stride % vw) continue;
+        if (pl.heads > 1 && pl.head_stride % vw) continue;
+        bool ok = true;
+        for (const auto &p : pl.pieces)
+            ok = ok && reinterpret_cast<uintptr_t>(p.strided) % uintptr_t(2 * vw) == 0;
+        if (ok) return vw;
+    }
+    return 1;
+}
+
+template <int VW, int FMT, bool kOne>
+int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
+    vf::QArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.codes = pl.codes;
+    a.scales = pl.scales;
+    a.row_stride = pl.row_stride;
+    a.head_stride = pl.head_stride;
+    a.d_stride = pl.d_stride;
+    a.heads = int32_t(pl.heads);
+    a.D = int32_t(pl.D);
+    a.lanes_log2 = lanes_log2;
+    a.nvec = int32_t(pl.D / VW);
+    const int64_t rows_per_block = int64_t(vf::kQuantThreads >> lanes_log2) * vf::kQuantRows;
+
+    const size_t n = pl.pieces.size();
+    for (size_t first = 0; first < n; first += vf::kMaxQPieces) {
+        const size_t cnt = std::min<size_t>(vf::kMaxQPieces, n - first);
+        int64_t max_hr = 0;
+        for (size_t i = 0; i < cnt; ++i) {
+            a.pieces[i] = pl.pieces[first + i];
+            max_hr = std::max(max_hr, a.pieces[i].rows * pl.heads);
+        }
+        if (max_hr == 0) continue;
+        cudaLaunchConfig_t cfg = {};
+        const int64_t gx = std::min(kMaxGridX, (max_hr + rows_per_block - 1) / rows_per_block);
+        cfg.gridDim = dim3(unsigned(gx), unsigned(cnt), 1);
+        cfg.blockDim = dim3(unsigned(vf::kQuantThreads), 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e;
+        if (pl.quantise)
+            e = cudaLaunchKernelEx(&cfg, vf::quantise_rows<VW, FMT, kOne>, a);
+        else
+            e = cudaLaunchKernelEx(&cfg, vf::dequantise_rows<VW, FMT>, a);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return VF_ERR_CUDA;
+        }
+    }
+    return VF_OK;
+}
+
+template <int VW, int FMT>
+int launch_vw(const Plan &pl, cudaStream_t stream) {
+    // group size: the smallest power of two covering the row's vectors, at most 32
+    const int64_t nvec = pl.D / VW;
+    int lg = 0;
+    while (lg < 5 && (int64_t(1) << lg) < nvec) ++lg;
+    const bool one = nvec <= (int64_t(1) << lg);
+    if (one || !pl.quantise) return launch_family<VW, FMT, true>(pl, lg, stream);
+    return launch_family<VW, FMT, false>(pl, lg, stream);
+}
+
+template <int FMT>
+int launch_fmt(const Plan &pl, int vw, cudaStream_t stream) {
+    switch (vw) {
+        case 8: return launch_vw<8, FMT>(pl, stream);
+        case 4: return launch_vw<4, FMT>(pl, stream);
+        case 2: return launch_vw<2, FMT>(pl, stream);
+        default: return launch_vw<1, FMT>(pl, stream);
+    }
+}
+
+}  // namespace
+
+int launch(const Plan &pl, cudaStream_t stream) {
+    if (pl.pieces.empty()) return VF_OK;
+    if (pl.heads > INT32_MAX || pl.D > INT32_MAX || pl.D < 1) return VF_ERR_ARG;
+    for (const auto &p : pl.pieces)
+        if (p.rows > INT32_MAX / std::max<int64_t>(pl.heads, 1)) return VF_ERR_ARG;
+    const int vw = pick_vector_width(pl);
+    if (pl.fmt == vf::kFmtInt8) return launch_fmt<vf::kFmtInt8>(pl, vw, stream);
+    if (pl.fmt == vf::kFmtE4M3) return launch_fmt<vf::kFmtE4M3>(pl, vw, stream);
+    return VF_ERR_ARG;
+}
+
+}  // namespace vfq

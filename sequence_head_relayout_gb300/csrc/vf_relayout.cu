@@ -19,6 +19,7 @@
 #include <utility>
 #include <vector>
 
+#include "quant.h"
 #include "relayout_kernel.cuh"
 #include "vf_relayout.h"
 
@@ -192,6 +193,8 @@ struct Request {
     int64_t str[3];                // strided view strides (token, head, d), elements
     int64_t heads_view;            // head extent of the strided view
     bool strided_written;          // merge, unpack
+    int fmt;                       // 0: exact 16-bit; else vf_format of the codes
+    float *scales;                 // lossy transport: one float per packed head row
 };
 
 // Block shape, vector width, grid order and launches.
@@ -203,6 +206,8 @@ int run(Request rq, cudaStream_t stream) {
     if (rc != VF_OK) return rc;
     if (rq.c_begin < 0 || rq.c_end < rq.c_begin || rq.c_end > s.C) return VF_ERR_ARG;
     if (rq.order != VF_ORDER_CHUNK_MAJOR && rq.order != VF_ORDER_SLOT_MAJOR) return VF_ERR_ARG;
+    if (rq.fmt != 0 && rq.fmt != VF_FORMAT_INT8 && rq.fmt != VF_FORMAT_E4M3) return VF_ERR_ARG;
+    const bool lossy = rq.fmt != 0;
     const int64_t slabs = slabs_of(s.op);
 
     // Geometry of one strided slab view [T][heads_view][D].
@@ -219,9 +224,12 @@ int run(Request rq, cudaStream_t stream) {
     const int64_t n = packed_elems(s);
     if (n == 0 || rq.c_begin == rq.c_end) return VF_OK;
 
-    // Pointers: present, 2-byte aligned, ranges inside the address space.
+    // Pointers: present, aligned (16-bit elements; codes are bytes, scales
+    // floats), ranges inside the address space.
     if (rq.packed == nullptr) return VF_ERR_ARG;
-    uintptr_t bits = reinterpret_cast<uintptr_t>(rq.packed);
+    if (lossy && (rq.scales == nullptr || reinterpret_cast<uintptr_t>(rq.scales) % 4u))
+        return VF_ERR_ARG;
+    uintptr_t bits = lossy ? 0 : reinterpret_cast<uintptr_t>(rq.packed);
     for (int64_t i = 0; i < slabs; ++i) {
         if (rq.strided[i] == nullptr) return VF_ERR_ARG;
         bits |= reinterpret_cast<uintptr_t>(rq.strided[i]);
@@ -229,13 +237,17 @@ int run(Request rq, cudaStream_t stream) {
     if (bits & 1u) return VF_ERR_ARG;
     if (rq.strided_written && !non_overlapping(ext, rq.str, 3)) return VF_ERR_ARG;
 
-    const Range packed{reinterpret_cast<uintptr_t>(rq.packed), uint64_t(2 * n)};
+    const Range packed{reinterpret_cast<uintptr_t>(rq.packed), uint64_t(lossy ? n : 2 * n)};
     if (packed.lo > UINTPTR_MAX - packed.len) return VF_ERR_OVERFLOW;
+    // n > 0 here, so D > 0; n / D head rows, 4 bytes each (n * 2 fits int64)
+    const Range scales{reinterpret_cast<uintptr_t>(rq.scales), lossy ? uint64_t(n / s.D) * 4 : 0};
+    if (scales.lo > UINTPTR_MAX - scales.len) return VF_ERR_OVERFLOW;
+    if (overlap(packed, scales)) return VF_ERR_ALIAS;
     Range views[3];
     for (int64_t i = 0; i < slabs; ++i) {
         views[i] = {reinterpret_cast<uintptr_t>(rq.strided[i]), uint64_t(view_bytes)};
         if (views[i].lo > UINTPTR_MAX - views[i].len) return VF_ERR_OVERFLOW;
-        if (overlap(packed, views[i])) return VF_ERR_ALIAS;
+        if (overlap(packed, views[i]) || overlap(scales, views[i])) return VF_ERR_ALIAS;
     }
     if (rq.strided_written)
         for (int64_t i = 0; i < slabs; ++i)
@@ -243,30 +255,29 @@ int run(Request rq, cudaStream_t stream) {
                 if (overlap(views[i], views[j])) return VF_ERR_ALIAS;
 
     if ((rc = check_pointer(rq.packed)) != VF_OK) return rc;
+    if (lossy && (rc = check_pointer(rq.scales)) != VF_OK) return rc;
     for (int64_t i = 0; i < slabs; ++i) {
         bool seen = false;
         for (int64_t j = 0; j < i; ++j) seen = seen || rq.strided[j] == rq.strided[i];
         if (!seen && (rc = check_pointer(rq.strided[i])) != VF_OK) return rc;
     }
 
-    Plan pl;
-    pl.packed = static_cast<uint16_t *>(rq.packed);
-    pl.row_stride = rq.str[0];
-    pl.head_stride = rq.str[1];
-    pl.d_stride = rq.str[2];
-    pl.heads = heads_per_row(s);
-    pl.D = s.D;
-    if (pl.heads > INT32_MAX || pl.D > INT32_MAX) return VF_ERR_ARG;
-    pl.piece_fastest = schedule_pieces_first(s.op);
-
     // Pieces of the requested chunks, one per (c, p, slab).  Pack and merge
     // address head group p of a full-head view; the split and the unpack
     // address all heads of their view.  A pack or unpack block holds its
     // q, k, v slabs back to back, each rows x heads x D.
+    const int64_t heads = heads_per_row(s);
+    if (heads > INT32_MAX || s.D > INT32_MAX) return VF_ERR_ARG;
     const std::vector<Entry> table = piece_table(s, rq.order);
     const int64_t group_heads = (s.op == VF_OP_QKV_PACK || s.op == VF_OP_HEAD_MERGE)
                                     ? s.H / s.P : 0;
-    const int64_t R = pl.heads * pl.D;
+    const int64_t R = heads * s.D;
+    struct Raw {
+        int64_t packed_off;
+        uint16_t *base;
+        int64_t rows;
+    };
+    std::vector<Raw> raw;
     for (int64_t c = rq.c_begin; c < rq.c_end; ++c)
         for (int64_t p = 0; p < s.P; ++p) {
             const Entry &e = table[size_t(c * s.P + p)];
@@ -277,13 +288,38 @@ int run(Request rq, cudaStream_t stream) {
             for (int64_t sl = 0; sl < slabs; ++sl) {
                 uint16_t *base = const_cast<uint16_t *>(
                     static_cast<const uint16_t *>(rq.strided[sl]));
-                pl.pieces.push_back({e.packed_off + sl * e.tok_len * R, base + off, e.tok_len});
+                raw.push_back({e.packed_off + sl * e.tok_len * R, base + off, e.tok_len});
             }
         }
-
-    if (pl.pieces.empty()) return VF_OK;
-    const int vw = pick_vector_width(pl);
+    if (raw.empty()) return VF_OK;
     const bool packed_is_dst = s.op == VF_OP_QKV_PACK || s.op == VF_OP_ATTN_SPLIT;
+
+    if (lossy) {
+        vfq::Plan q;
+        q.codes = static_cast<uint8_t *>(rq.packed);
+        q.scales = rq.scales;
+        q.row_stride = rq.str[0];
+        q.head_stride = rq.str[1];
+        q.d_stride = rq.str[2];
+        q.heads = heads;
+        q.D = s.D;
+        q.fmt = rq.fmt;
+        q.quantise = packed_is_dst;
+        // block offsets are whole head rows: multiples of D
+        for (const Raw &r : raw) q.pieces.push_back({r.packed_off / s.D, r.base, r.rows});
+        return vfq::launch(q, stream);
+    }
+
+    Plan pl;
+    pl.packed = static_cast<uint16_t *>(rq.packed);
+    pl.row_stride = rq.str[0];
+    pl.head_stride = rq.str[1];
+    pl.d_stride = rq.str[2];
+    pl.heads = heads;
+    pl.D = s.D;
+    pl.piece_fastest = schedule_pieces_first(s.op);
+    for (const Raw &r : raw) pl.pieces.push_back({r.packed_off, r.base, r.rows});
+    const int vw = pick_vector_width(pl);
     return packed_is_dst ? launch_dir<true>(pl, vw, stream) : launch_dir<false>(pl, vw, stream);
 }
 
@@ -298,8 +334,11 @@ int64_t range_end(int64_t c_begin, int64_t c_count) {
 
 int pack_common(const void *q, const void *k, const void *v, const int64_t *str,
                 int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, int64_t c_begin,
-                int64_t c_count, void *dst, vf_stream_t stream) {
+                int64_t c_count, void *dst, vf_stream_t stream, int fmt = 0,
+                float *scales = nullptr) {
     Request rq{};
+    rq.fmt = fmt;
+    rq.scales = scales;
     rq.s = {VF_OP_QKV_PACK, T, H, D, P, C};
     rq.c_begin = c_begin;
     rq.c_end = range_end(c_begin, c_count);
@@ -315,14 +354,14 @@ int pack_common(const void *q, const void *k, const void *v, const int64_t *str,
 
 int pack4(const void *src, const int64_t src_strides[4], int64_t T, int64_t H, int64_t D,
           int64_t P, int64_t C, int64_t c_begin, int64_t c_count, void *dst,
-          vf_stream_t stream) {
+          vf_stream_t stream, int fmt = 0, float *scales = nullptr) {
     if (src_strides == nullptr) return VF_ERR_ARG;
     const int64_t ss = src_strides[1];
     if (ss < 0) return VF_ERR_ARG;
     const int64_t str[3] = {src_strides[0], src_strides[2], src_strides[3]};
     if (src == nullptr)      // only legal when nothing is moved; run() decides
         return pack_common(nullptr, nullptr, nullptr, str, T, H, D, P, C, c_begin, c_count,
-                           dst, stream);
+                           dst, stream, fmt, scales);
     // slab s of the [T][3][H][D] view starts s * ss elements after src
     int64_t off2;
     if (!mul_ok(ss, 4, &off2)) return VF_ERR_OVERFLOW;                 // 2 slabs x 2 bytes
@@ -330,14 +369,16 @@ int pack4(const void *src, const int64_t src_strides[4], int64_t T, int64_t H, i
     if (base > UINTPTR_MAX - uint64_t(off2)) return VF_ERR_OVERFLOW;
     const char *b = static_cast<const char *>(src);
     return pack_common(src, b + 2 * ss, b + 4 * ss, str, T, H, D, P, C, c_begin, c_count, dst,
-                       stream);
+                       stream, fmt, scales);
 }
 
 int split_common(const void *src, const int64_t src_strides[3], int64_t T, int64_t H,
                  int64_t D, int64_t P, int64_t C, int64_t c_begin, int64_t c_count, void *dst,
-                 vf_stream_t stream) {
+                 vf_stream_t stream, int fmt = 0, float *scales = nullptr) {
     if (src_strides == nullptr) return VF_ERR_ARG;
     Request rq{};
+    rq.fmt = fmt;
+    rq.scales = scales;
     rq.s = {VF_OP_ATTN_SPLIT, T, H, D, P, C};
     rq.c_begin = c_begin;
     rq.c_end = range_end(c_begin, c_count);
@@ -351,8 +392,10 @@ int split_common(const void *src, const int64_t src_strides[3], int64_t T, int64
 
 int merge_common(const void *src, const int64_t dst_strides[3], int64_t T, int64_t H,
                  int64_t D, int64_t P, int64_t C, int64_t c_begin, int64_t c_count, void *dst,
-                 vf_stream_t stream) {
+                 vf_stream_t stream, int fmt = 0, const float *scales = nullptr) {
     Request rq{};
+    rq.fmt = fmt;
+    rq.scales = const_cast<float *>(scales);
     rq.s = {VF_OP_HEAD_MERGE, T, H, D, P, C};
     rq.c_begin = c_begin;
     rq.c_end = range_end(c_begin, c_count);
@@ -372,9 +415,12 @@ int merge_common(const void *src, const int64_t dst_strides[3], int64_t T, int64
 
 int unpack_common(const void *recv, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C,
                   int64_t c_begin, int64_t c_count, void *q, void *k, void *v,
-                  const int64_t out_strides[3], vf_stream_t stream) {
+                  const int64_t out_strides[3], vf_stream_t stream, int fmt = 0,
+                  const float *scales = nullptr) {
     if (P < 1 || H < 0 || D < 0 || H % P != 0) return VF_ERR_ARG;
     Request rq{};
+    rq.fmt = fmt;
+    rq.scales = const_cast<float *>(scales);
     rq.s = {VF_OP_QKV_UNPACK, T, H, D, P, C};
     rq.c_begin = c_begin;
     rq.c_end = range_end(c_begin, c_count);
@@ -392,6 +438,26 @@ int unpack_common(const void *recv, int64_t T, int64_t H, int64_t D, int64_t P, 
     }
     rq.heads_view = Hp;
     rq.strided_written = true;
+    return run(rq, as_stream(stream));
+}
+
+// vf_relayout and vf_relayout_q: map the descriptor onto a Request.
+int relayout_desc(const vf_relayout_desc *d, int fmt, float *scales, vf_stream_t stream) {
+    Request rq{};
+    rq.fmt = fmt;
+    rq.scales = scales;
+    rq.s = {d->op, d->T, d->H, d->D, d->P, d->C};
+    if (!is_op(d->op)) return VF_ERR_ARG;
+    rq.order = d->order;
+    rq.c_begin = d->c_begin;
+    rq.c_end = range_end(d->c_begin, d->c_count);
+    rq.packed = d->packed;
+    const int64_t slabs = slabs_of(d->op);
+    for (int i = 0; i < 3; ++i) rq.strided[i] = i < slabs ? d->strided[i] : nullptr;
+    for (int i = 0; i < 3; ++i) rq.str[i] = d->strides[i];
+    if (d->P < 1 || d->H < 0) return VF_ERR_ARG;
+    rq.heads_view = d->op == VF_OP_QKV_UNPACK ? d->H / d->P : d->H;
+    rq.strided_written = d->op == VF_OP_HEAD_MERGE || d->op == VF_OP_QKV_UNPACK;
     return run(rq, as_stream(stream));
 }
 
@@ -482,22 +548,49 @@ int64_t vf_piece_table(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64
                              packed_off, cap);
 }
 
+int vf_relayout_q(const vf_relayout_desc *d, int format, float *scales, vf_stream_t stream) {
+    if (d == nullptr || (format != VF_FORMAT_INT8 && format != VF_FORMAT_E4M3))
+        return VF_ERR_ARG;
+    return relayout_desc(d, format, scales, stream);
+}
+
 int vf_relayout(const vf_relayout_desc *d, vf_stream_t stream) {
     if (d == nullptr) return VF_ERR_ARG;
-    Request rq{};
-    rq.s = {d->op, d->T, d->H, d->D, d->P, d->C};
-    if (!is_op(d->op)) return VF_ERR_ARG;
-    rq.order = d->order;
-    rq.c_begin = d->c_begin;
-    rq.c_end = range_end(d->c_begin, d->c_count);
-    rq.packed = d->packed;
-    const int64_t slabs = slabs_of(d->op);
-    for (int i = 0; i < 3; ++i) rq.strided[i] = i < slabs ? d->strided[i] : nullptr;
-    for (int i = 0; i < 3; ++i) rq.str[i] = d->strides[i];
-    if (d->P < 1 || d->H < 0) return VF_ERR_ARG;
-    rq.heads_view = d->op == VF_OP_QKV_UNPACK ? d->H / d->P : d->H;
-    rq.strided_written = d->op == VF_OP_HEAD_MERGE || d->op == VF_OP_QKV_UNPACK;
-    return run(rq, as_stream(stream));
+    return relayout_desc(d, 0, nullptr, stream);
+}
+
+int vf_qkv_pack_int8(const void *src, const int64_t src_strides[4], int64_t T, int64_t H,
+                     int64_t D, int64_t P, int64_t C, void *codes, float *scales,
+                     vf_stream_t stream) {
+    return pack4(src, src_strides, T, H, D, P, C, 0, C, codes, stream, VF_FORMAT_INT8, scales);
+}
+
+int vf_qkv_unpack_int8(const void *codes, const float *scales, int64_t T, int64_t H, int64_t D,
+                       int64_t P, int64_t C, void *q, void *k, void *v,
+                       const int64_t out_strides[3], vf_stream_t stream) {
+    return unpack_common(codes, T, H, D, P, C, 0, C, q, k, v, out_strides, stream,
+                         VF_FORMAT_INT8, scales);
+}
+
+int vf_attn_split_fp8(const void *src, const int64_t src_strides[3], int64_t T, int64_t H,
+                      int64_t D, int64_t P, int64_t C, void *codes, float *scales,
+                      vf_stream_t stream) {
+    return split_common(src, src_strides, T, H, D, P, C, 0, C, codes, stream, VF_FORMAT_E4M3,
+                        scales);
+}
+
+int vf_head_merge_fp8(const void *codes, const float *scales, const int64_t dst_strides[3],
+                      int64_t T, int64_t H, int64_t D, int64_t P, int64_t C, void *dst,
+                      vf_stream_t stream) {
+    return merge_common(codes, dst_strides, T, H, D, P, C, 0, C, dst, stream, VF_FORMAT_E4M3,
+                        scales);
+}
+
+int64_t vf_scale_count(int op, int64_t T, int64_t H, int64_t D, int64_t P, int64_t C) {
+    const Shape s{op, T, H, D, P, C};
+    const int rc = check_shape(s);
+    if (rc != VF_OK) return rc;
+    return D == 0 ? 0 : packed_elems(s) / D;
 }
 
 const char *vf_status_string(int status) {

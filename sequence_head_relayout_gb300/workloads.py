@@ -175,3 +175,37 @@ def merge_destination(cfg: Config, device="cpu", fill: int = None):
     else:
         raise ValueError(cfg.merge_dst)
     return view, base
+
+
+def finite_rows_(view: torch.Tensor, seed: int) -> torch.Tensor:
+    """Fill a 16-bit view [..., D] in place with finite bf16 rows for the
+    lossy transport: each D-element row is N(0,1) draws times 2^k, k a seeded
+    integer in [-24, 24] (rows of very different magnitude), with planted
+    rows: all +0, all -0 and +0 mixed, a row scaled by 2^-100 (below the
+    quantiser's 2^-96 floor), a row whose largest magnitude is exactly 2^-96,
+    and rows mixing bf16 denormals with normal values."""
+    D = view.shape[-1]
+    rows = view.numel() // D if D else 0
+    if rows == 0:
+        return view
+    g = torch.Generator(device=view.device)
+    g.manual_seed(seed)
+    x = torch.randn((rows, D), generator=g, device=view.device, dtype=torch.float32)
+    k = torch.randint(-24, 25, (rows, 1), generator=g, device=view.device)
+    x = x * torch.pow(2.0, k.to(torch.float32))
+    step = max(1, rows // 53)
+    for j, r in enumerate(range(0, rows, step)):
+        kind = j % 5
+        if kind == 0:
+            x[r] = 0.0
+        elif kind == 1:
+            x[r] = torch.where(torch.arange(D, device=view.device) % 2 == 0, -0.0, 0.0)
+        elif kind == 2:
+            x[r] = x[r] / x[r].abs().max().clamp_min(1e-30) * 2.0 ** -100
+        elif kind == 3:
+            x[r] = x[r] / x[r].abs().max().clamp_min(1e-30) * 2.0 ** -97
+            x[r, 0] = 2.0 ** -96
+        else:
+            x[r, ::3] = 2.0 ** -130                       # bf16 denormal
+    view.copy_(x.to(torch.bfloat16).view(torch.int16).view(view.shape))
+    return view
