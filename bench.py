@@ -86,6 +86,12 @@ def alg_bytes(elems: int) -> int:
     return 2 * 2 * elems            # read once + written once, 2 bytes each
 
 
+def lossy_bytes(elems: int, D: int) -> int:
+    """Lossy transport: 2 B bf16 + 1 B code per element, plus one 4 B scale
+    per D-element head row (read or written once each)."""
+    return 3 * elems + 4 * (elems // D)
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle (reported baseline and reference arm); runs in spawned workers
 # ----------------------------------------------------------------------------
@@ -448,6 +454,13 @@ def gpu_arm(args, rank, world, local_rank):
         e2e = e2e_arm(args, cfg, dev, world)
 
     configs = per_config(args, dev) if args.configs else None
+    lossy = None
+    if configs and cfg.name in configs["table"]:
+        row = configs["table"][cfg.name]
+        lossy = {k: row[k] for k in ("qkv_pack_int8", "qkv_unpack_int8", "attn_split_e4m3",
+                                     "head_merge_e4m3")}
+        lossy["note"] = ("opt-in INT8 QKV / E4M3 attention-output transport at the bench "
+                         "workload; GB/s counts 3 B per element + 4 B per head row")
     chain_aba = None if args.no_chain else torch_chain_aba(cfg, dev)
 
     line = None
@@ -474,6 +487,7 @@ def gpu_arm(args, rank, world, local_rank):
             "gpu_launches": K * launches_per_step(cfg, ops_run),
             "e2e": e2e,
             "per_config": configs,
+            "lossy_transport": lossy,
             "vs_torch_chain": chain_aba,
         }
     return line
@@ -783,23 +797,43 @@ def per_config(args, dev):
         outs = tuple(torch.empty((T, Hp, D), dtype=torch.int16, device=dev) for _ in range(3))
         pack_dst = torch.empty(3 * T * H * D, dtype=torch.int16, device=dev)
         split_dst = torch.empty(T * H * D, dtype=torch.int16, device=dev)
+        n_pack, n_split, n_unpack = 3 * T * H * D, T * H * D, 3 * T * Hp * D
+        # opt-in lossy transport: codes + one float scale per head row
+        q_pack = torch.empty(n_pack, dtype=torch.int8, device=dev)
+        q_pack_s = torch.empty(n_pack // D, dtype=torch.float32, device=dev)
+        q_split = torch.empty(n_split, dtype=torch.float8_e4m3fn, device=dev)
+        q_split_s = torch.empty(n_split // D, dtype=torch.float32, device=dev)
+        vf.qkv_pack_q(pack_src, P, C, fmt="int8", codes=q_pack, scales=q_pack_s)
+        vf.attn_split_q(split_src, P, C, fmt="e4m3", codes=q_split, scales=q_split_s)
+        q_recv, q_recv_s = q_pack[:n_unpack], q_pack_s[:n_unpack // D]
+        merge_bf16 = merge_dst.view(torch.bfloat16)
+        outs_bf16 = tuple(o.view(torch.bfloat16) for o in outs)
         ops = {
-            "qkv_pack": (3 * T * H * D,
+            "qkv_pack": (alg_bytes(n_pack),
                          lambda: vf.qkv_pack(pack_src, P, C, out=pack_dst)),
-            "attn_split": (T * H * D, lambda: vf.attn_split(split_src, P, C, out=split_dst)),
-            "head_merge": (T * H * D, lambda: vf.head_merge(merge_src, T, H, D, P, C,
-                                                             out=merge_dst)),
-            "qkv_unpack": (3 * T * Hp * D, lambda: vf.qkv_unpack(recv, T, H, D, P, C,
-                                                                 outs=outs)),
-            "qkv_pack3": (3 * T * H * D, lambda: vf.qkv_pack3(
+            "attn_split": (alg_bytes(n_split),
+                           lambda: vf.attn_split(split_src, P, C, out=split_dst)),
+            "head_merge": (alg_bytes(n_split), lambda: vf.head_merge(merge_src, T, H, D, P, C,
+                                                                     out=merge_dst)),
+            "qkv_unpack": (alg_bytes(n_unpack), lambda: vf.qkv_unpack(recv, T, H, D, P, C,
+                                                                      outs=outs)),
+            "qkv_pack3": (alg_bytes(n_pack), lambda: vf.qkv_pack3(
                 pack_src[:, 0], pack_src[:, 1], pack_src[:, 2], P, C, out=pack_dst)),
-            "qkv_pack_slot_major": (3 * T * H * D, lambda: vf.qkv_pack(
+            "qkv_pack_slot_major": (alg_bytes(n_pack), lambda: vf.qkv_pack(
                 pack_src, P, C, out=pack_dst, order="slot_major")),
-            "head_merge_slot_major": (T * H * D, lambda: vf.head_merge(
+            "head_merge_slot_major": (alg_bytes(n_split), lambda: vf.head_merge(
                 merge_src, T, H, D, P, C, out=merge_dst, order="slot_major")),
+            "qkv_pack_int8": (lossy_bytes(n_pack, D), lambda: vf.qkv_pack_q(
+                pack_src, P, C, fmt="int8", codes=q_pack, scales=q_pack_s)),
+            "qkv_unpack_int8": (lossy_bytes(n_unpack, D), lambda: vf.qkv_unpack_q(
+                q_recv, q_recv_s, T, H, D, P, C, fmt="int8", outs=outs_bf16)),
+            "attn_split_e4m3": (lossy_bytes(n_split, D), lambda: vf.attn_split_q(
+                split_src, P, C, fmt="e4m3", codes=q_split, scales=q_split_s)),
+            "head_merge_e4m3": (lossy_bytes(n_split, D), lambda: vf.head_merge_q(
+                q_split, q_split_s, T, H, D, P, C, fmt="e4m3", out=merge_bf16)),
         }
         row = {}
-        for op, (elems, fn) in ops.items():
+        for op, (nbytes, fn) in ops.items():
             for _ in range(3):
                 fn()
             ts = []
@@ -813,13 +847,17 @@ def per_config(args, dev):
                 ts.append((a, b))
             torch.cuda.synchronize()
             med = statistics.median(x.elapsed_time(y) for x, y in ts)
-            gbs = alg_bytes(elems) / (med / 1e3) / 1e9
+            gbs = nbytes / (med / 1e3) / 1e9
             row[op] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
                        "frac_of_peak": round(gbs / peak, 4)}
         table[name] = row
         del pack_src, split_src, merge_src, merge_dst, recv, outs, pack_dst, split_dst
+        del q_pack, q_pack_s, q_split, q_split_s, q_recv, q_recv_s, merge_bf16, outs_bf16
         torch.cuda.empty_cache()
     return {"reps": reps, "l2": "256 MB buffer written between reps, outside the events",
+            "bytes": "exact ops: 4 B per element (2 read, 2 written); *_int8 / *_e4m3 "
+                     "(opt-in lossy transport): 3 B per element plus one 4 B scale per "
+                     "D-element head row",
             "table": table}
 
 

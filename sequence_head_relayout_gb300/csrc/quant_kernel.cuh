@@ -29,6 +29,25 @@
 // |x| is the integer order of those bits).  Each group keeps kQuantRows head
 // rows' loads in flight.  Blocks are kQuantThreads threads, whole warps, so
 // every shuffle runs with all 32 lanes present.
+//
+// The kernels are bound by instruction issue before HBM unless every
+// per-element step is a single cheap instruction, so the 8-element path
+// (quantise_rows8 / dequantise_rows8) uses exact integer tricks in place of
+// conversion instructions, each equal to the plain float32 step:
+//   * round half to even to an integer: fl(q + 1.5 * 2^23) for |q| < 2^22 is
+//     1.5 * 2^23 + rint(q) (the sum's unit in the last place is 1 and the
+//     addition itself rounds to nearest even; 1.5 * 2^23 is even), and its
+//     low byte is rint(q) as a two's-complement byte.  No clamp is needed:
+//     |x| <= amax gives |q| <= 127 (1 + 2^-24)^2 < 127.5, so rint(q) is within
+//     +-127 (a clamp there would never act);
+//   * int8 code to float: the float with bits 0x4B000000 | (c ^ 0x80) is
+//     2^23 + c + 128 exactly; subtracting 2^23 + 128 gives c exactly;
+//   * magnitudes: max over |x| in the integer order of the 15 magnitude bits,
+//     two at a time with the 16-bit-lane max of sm_90+;
+//   * the row index (token, head) of a group: n / heads by a multiply-high
+//     and a shift (the round-up method of Granlund and Montgomery, "Division
+//     by invariant integers using multiplication", 1994), exact for
+//     n < 2^31.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -66,6 +85,8 @@ struct QArgs {
     int32_t D;             // elements per head row
     int32_t lanes_log2;    // group size G = 1 << lanes_log2
     int32_t nvec;          // ceil(D / VW) vectors per head row
+    uint32_t div_mul;      // n / heads == (umulhi(n, div_mul) + n) >> div_shift, n < 2^31
+    uint32_t div_shift;
     QPiece pieces[kMaxQPieces];
 };
 
@@ -131,10 +152,78 @@ __device__ __forceinline__ uint32_t magnitude_max(const uint16_t (&h)[VW]) {
 
 // Position of head row hr of a piece: (token, head) -> strided element offset.
 __device__ __forceinline__ int64_t strided_offset(const QArgs &a, uint32_t hr, int64_t e) {
-    const uint32_t heads = uint32_t(a.heads);
-    const uint32_t t = hr / heads;
-    const uint32_t hh = hr - t * heads;
+    const uint32_t t = (__umulhi(hr, a.div_mul) + hr) >> a.div_shift;   // hr / heads
+    const uint32_t hh = hr - t * uint32_t(a.heads);
     return int64_t(t) * a.row_stride + int64_t(hh) * a.head_stride + e * a.d_stride;
+}
+
+// Per 16-bit lane maximum of two words (sm_90+).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Both 15-bit magnitudes of a word of two bfloat16 patterns, lane-wise.
+__device__ __forceinline__ uint32_t mag2(uint32_t w) { return w & 0x7FFF7FFFu; }
+
+// Low byte of the integer nearest to q (ties to even), for |q| < 2^22.
+__device__ __forceinline__ uint32_t rint_bits(float q) {
+    return __float_as_uint(__fadd_rn(q, 12582912.0f));
+}
+
+// Eight bfloat16 patterns -> eight codes.
+template <int FMT>
+__device__ __forceinline__ uint2 encode8(const uint4 &w, float inv) {
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float f[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t x = in[2 * k + j];
+            f[2 * j] = __fmul_rn(__uint_as_float(x << 16), inv);          // element 2j
+            f[2 * j + 1] = __fmul_rn(__uint_as_float(x & 0xFFFF0000u), inv);
+        }
+        if constexpr (FMT == kFmtInt8) {
+            const uint32_t b01 = __byte_perm(rint_bits(f[0]), rint_bits(f[1]), 0x0040);
+            const uint32_t b23 = __byte_perm(rint_bits(f[2]), rint_bits(f[3]), 0x0040);
+            out[k] = __byte_perm(b01, b23, 0x5410);
+        } else {
+            const uint32_t p01 = __nv_cvt_float2_to_fp8x2(make_float2(f[0], f[1]),
+                                                          __NV_SATFINITE, __NV_E4M3);
+            const uint32_t p23 = __nv_cvt_float2_to_fp8x2(make_float2(f[2], f[3]),
+                                                          __NV_SATFINITE, __NV_E4M3);
+            out[k] = __byte_perm(p01, p23, 0x5410);
+        }
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+// Four codes (one word) times the scale -> four bfloat16 patterns (two words).
+template <int FMT>
+__device__ __forceinline__ uint2 decode4(uint32_t c, float s) {
+    float f[4];
+    if constexpr (FMT == kFmtInt8) {
+        const uint32_t u = c ^ 0x80808080u;                  // c + 128, per byte
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f[i] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u | i)),
+                             8388736.0f);                    // 2^23 + 128
+    } else {
+        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(c & 0xFFFFu),
+                                                          __NV_E4M3);
+        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(c >> 16),
+                                                          __NV_E4M3);
+        const float2 a = __half22float2(__half2(lo));       // exact: E4M3 fits in half
+        const float2 b = __half22float2(__half2(hi));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    }
+    const __nv_bfloat162 y01 = __floats2bfloat162_rn(__fmul_rn(f[0], s), __fmul_rn(f[1], s));
+    const __nv_bfloat162 y23 = __floats2bfloat162_rn(__fmul_rn(f[2], s), __fmul_rn(f[3], s));
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&y01),
+                      *reinterpret_cast<const uint32_t *>(&y23));
 }
 
 __device__ __forceinline__ void wait_for_previous_grid() {
@@ -293,6 +382,118 @@ dequantise_rows(const __grid_constant__ QArgs a) {
                     memcpy(&out, y, sizeof(out));
                     *reinterpret_cast<B *>(row + int64_t(v) * VW * a.d_stride) = out;
                 }
+            }
+        }
+    }
+}
+
+// 8-element vectors (D % 8 == 0, d contiguous, aligned): NV vectors per
+// lane, vector j of lane l at index l + j * G of the head row, so that each
+// of a warp's loads covers consecutive 16-byte pieces.
+template <int FMT, int NV>
+__global__ void __launch_bounds__(kQuantThreads)
+quantise_rows8(const __grid_constant__ QArgs a) {
+    wait_for_previous_grid();
+    const QPiece &pc = a.pieces[blockIdx.y];
+    const uint32_t G = 1u << a.lanes_log2;
+    const uint32_t lane = threadIdx.x & (G - 1);
+    const uint32_t groups = kQuantThreads >> a.lanes_log2;
+    const uint32_t group = threadIdx.x >> a.lanes_log2;
+    const uint32_t nrows = uint32_t(pc.rows) * uint32_t(a.heads);   // < 2^31, host-checked
+    const uint32_t nvec = uint32_t(a.nvec);
+    const float top = top_code<FMT>();
+
+    for (uint32_t base = blockIdx.x * groups * kQuantRows; base < nrows;
+         base += gridDim.x * groups * kQuantRows) {
+        uint4 w[kQuantRows][NV];
+        uint32_t m[kQuantRows];
+#pragma unroll
+        for (int r = 0; r < kQuantRows; ++r) {
+            const uint32_t hr = base + group + uint32_t(r) * groups;
+            const uint16_t *row = pc.strided + strided_offset(a, hr, 0);
+            m[r] = 0;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const uint32_t v = lane + uint32_t(j) * G;
+                w[r][j] = make_uint4(0, 0, 0, 0);
+                if (hr < nrows && v < nvec)
+                    w[r][j] = *reinterpret_cast<const uint4 *>(row + int64_t(v) * 8);
+                m[r] = max_u16x2(m[r], max_u16x2(max_u16x2(mag2(w[r][j].x), mag2(w[r][j].y)),
+                                                 max_u16x2(mag2(w[r][j].z), mag2(w[r][j].w))));
+            }
+        }
+        // group-wide amax: all 32 lanes of every warp are here
+#pragma unroll
+        for (int r = 0; r < kQuantRows; ++r) {
+            for (uint32_t o = G >> 1; o > 0; o >>= 1)
+                m[r] = max_u16x2(m[r], __shfl_xor_sync(0xFFFFFFFFu, m[r], int(o)));
+            m[r] = max(m[r] & 0xFFFFu, m[r] >> 16);
+        }
+#pragma unroll
+        for (int r = 0; r < kQuantRows; ++r) {
+            const uint32_t hr = base + group + uint32_t(r) * groups;
+            if (hr >= nrows) continue;
+            const float amax = bf16_bits_to_float(m[r]);
+            const bool live = amax >= 0x1p-96f;
+            const float inv = live ? __fdiv_rn(top, amax) : 0.0f;
+            const int64_t prow = pc.first_row + hr;               // packed head row
+            uint8_t *crow = a.codes + prow * a.D;
+            if (lane == 0) a.scales[prow] = live ? __fdiv_rn(amax, top) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const uint32_t v = lane + uint32_t(j) * G;
+                if (v >= nvec) continue;
+                uint2 c = encode8<FMT>(w[r][j], inv);
+                if (!live) c = make_uint2(0, 0);
+                *reinterpret_cast<uint2 *>(crow + int64_t(v) * 8) = c;
+            }
+        }
+    }
+}
+
+template <int FMT, int NV>
+__global__ void __launch_bounds__(kQuantThreads)
+dequantise_rows8(const __grid_constant__ QArgs a) {
+    wait_for_previous_grid();
+    const QPiece &pc = a.pieces[blockIdx.y];
+    const uint32_t G = 1u << a.lanes_log2;
+    const uint32_t lane = threadIdx.x & (G - 1);
+    const uint32_t groups = kQuantThreads >> a.lanes_log2;
+    const uint32_t group = threadIdx.x >> a.lanes_log2;
+    const uint32_t nrows = uint32_t(pc.rows) * uint32_t(a.heads);
+    const uint32_t nvec = uint32_t(a.nvec);
+
+    for (uint32_t base = blockIdx.x * groups * kQuantRows; base < nrows;
+         base += gridDim.x * groups * kQuantRows) {
+        uint2 c[kQuantRows][NV];
+        float sc[kQuantRows];
+#pragma unroll
+        for (int r = 0; r < kQuantRows; ++r) {
+            const uint32_t hr = base + group + uint32_t(r) * groups;
+            const int64_t prow = pc.first_row + hr;
+            sc[r] = hr < nrows ? a.scales[prow] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const uint32_t v = lane + uint32_t(j) * G;
+                c[r][j] = make_uint2(0, 0);
+                if (hr < nrows && v < nvec)
+                    c[r][j] = *reinterpret_cast<const uint2 *>(a.codes + prow * a.D +
+                                                               int64_t(v) * 8);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kQuantRows; ++r) {
+            const uint32_t hr = base + group + uint32_t(r) * groups;
+            if (hr >= nrows) continue;
+            uint16_t *row = pc.strided + strided_offset(a, hr, 0);
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const uint32_t v = lane + uint32_t(j) * G;
+                if (v >= nvec) continue;
+                const uint2 lo = decode4<FMT>(c[r][j].x, sc[r]);
+                const uint2 hi = decode4<FMT>(c[r][j].y, sc[r]);
+                *reinterpret_cast<uint4 *>(row + int64_t(v) * 8) =
+                    make_uint4(lo.x, lo.y, hi.x, hi.y);
             }
         }
     }

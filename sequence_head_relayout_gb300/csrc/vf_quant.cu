@@ -20,6 +20,25 @@ static_assert(vf::kFmtInt8 == VF_FORMAT_INT8 && vf::kFmtE4M3 == VF_FORMAT_E4M3,
 
 constexpr int64_t kMaxGridX = int64_t(1) << 20;   // the kernels stride over head rows
 
+// 16-byte vectors per lane on the 8-element path (tuning constant, measured
+// on GB300).
+#ifndef VF_QUANT_NV
+#define VF_QUANT_NV 2
+#endif
+constexpr int kNV = VF_QUANT_NV;
+
+// Multiplier and shift with n / d == (umulhi(n, mul) + n) >> shift for all
+// n < 2^31 and 1 <= d < 2^31 (Granlund and Montgomery's round-up method):
+// shift = ceil(log2 d), mul = floor(2^32 (2^shift - d) / d) + 1 < 2^32.
+void fast_divisor(int64_t d, uint32_t *mul, uint32_t *shift) {
+    uint32_t l = 0;
+    while ((int64_t(1) << l) < d) ++l;
+    const unsigned __int128 num = (static_cast<unsigned __int128>(1) << 32) *
+                                  static_cast<unsigned __int128>((int64_t(1) << l) - d);
+    *mul = uint32_t(num / static_cast<unsigned __int128>(d) + 1);
+    *shift = l;
+}
+
 // Widest vector (elements) that keeps every access of both sides aligned:
 // codes need VW-byte alignment (row starts are multiples of D), the
 // strided side 2*VW bytes.
@@ -39,7 +58,9 @@ int pick_vector_width(const Plan &pl) {
     return 1;
 }
 
-template <int VW, int FMT, bool kOne>
+// kPath: 0 = generic, one vector per lane; 1 = generic, per-lane loop;
+// 2 = the 8-element path with kNV vectors per lane.
+template <int VW, int FMT, int kPath>
 int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
     vf::QArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -52,6 +73,7 @@ int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
     a.D = int32_t(pl.D);
     a.lanes_log2 = lanes_log2;
     a.nvec = int32_t(pl.D / VW);
+    fast_divisor(std::max<int64_t>(pl.heads, 1), &a.div_mul, &a.div_shift);
     const int64_t rows_per_block = int64_t(vf::kQuantThreads >> lanes_log2) * vf::kQuantRows;
 
     const size_t n = pl.pieces.size();
@@ -75,10 +97,17 @@ int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         cudaError_t e;
-        if (pl.quantise)
-            e = cudaLaunchKernelEx(&cfg, vf::quantise_rows<VW, FMT, kOne>, a);
-        else
-            e = cudaLaunchKernelEx(&cfg, vf::dequantise_rows<VW, FMT>, a);
+        if constexpr (kPath == 2) {
+            if (pl.quantise)
+                e = cudaLaunchKernelEx(&cfg, vf::quantise_rows8<FMT, kNV>, a);
+            else
+                e = cudaLaunchKernelEx(&cfg, vf::dequantise_rows8<FMT, kNV>, a);
+        } else {
+            if (pl.quantise)
+                e = cudaLaunchKernelEx(&cfg, vf::quantise_rows<VW, FMT, kPath == 0>, a);
+            else
+                e = cudaLaunchKernelEx(&cfg, vf::dequantise_rows<VW, FMT>, a);
+        }
         if (e != cudaSuccess) {
             cudaGetLastError();
             return VF_ERR_CUDA;
@@ -87,15 +116,23 @@ int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
     return VF_OK;
 }
 
+// Group size: the smallest power of two of lanes, at most 32, that covers the
+// row's vectors at `per_lane` vectors each.
+int lanes_log2_for(int64_t nvec, int64_t per_lane) {
+    int lg = 0;
+    while (lg < 5 && (int64_t(1) << lg) * per_lane < nvec) ++lg;
+    return lg;
+}
+
 template <int VW, int FMT>
 int launch_vw(const Plan &pl, cudaStream_t stream) {
-    // group size: the smallest power of two covering the row's vectors, at most 32
     const int64_t nvec = pl.D / VW;
-    int lg = 0;
-    while (lg < 5 && (int64_t(1) << lg) < nvec) ++lg;
+    if (VW == 8 && nvec <= 32 * kNV)
+        return launch_family<VW, FMT, 2>(pl, lanes_log2_for(nvec, kNV), stream);
+    const int lg = lanes_log2_for(nvec, 1);
     const bool one = nvec <= (int64_t(1) << lg);
-    if (one || !pl.quantise) return launch_family<VW, FMT, true>(pl, lg, stream);
-    return launch_family<VW, FMT, false>(pl, lg, stream);
+    if (one || !pl.quantise) return launch_family<VW, FMT, 0>(pl, lg, stream);
+    return launch_family<VW, FMT, 1>(pl, lg, stream);
 }
 
 template <int FMT>
