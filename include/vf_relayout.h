@@ -26,7 +26,8 @@
  *   (c, p) for c = 0..C-1 (outer), p = 0..P-1 (inner), no gaps, no padding.
  *   vf_relayout can also place the same blocks p outer (vf_order).
  *
- * Elements are 16-bit (BF16) and are moved as raw bit patterns: NaN payloads,
+ * Elements are 16-bit (BF16) and are moved as raw bit patterns (the opt-in
+ * lossy transport at the end of this file quantises instead): NaN payloads,
  * -0 and denormals arrive unchanged.  Strides are in ELEMENTS, int64, and
  * must be non-negative.  All offsets are computed in 64-bit arithmetic.
  *

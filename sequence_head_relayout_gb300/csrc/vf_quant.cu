@@ -20,12 +20,19 @@ static_assert(vf::kFmtInt8 == VF_FORMAT_INT8 && vf::kFmtE4M3 == VF_FORMAT_E4M3,
 
 constexpr int64_t kMaxGridX = int64_t(1) << 20;   // the kernels stride over head rows
 
-// 16-byte vectors per lane on the 8-element path (tuning constant, measured
-// on GB300).
+// 16-byte vectors per lane on the 8-element path, quantising and
+// dequantising (tuning constants).  Measured on GB300 over 1, 2 and 4 vectors
+// and 1, 2 and 4 head rows in flight per group: quantising is fastest at 4
+// vectors and 2 rows (the per-row reduction and divisions amortised over 32
+// elements per lane), dequantising at 2 vectors and 1-2 rows.
 #ifndef VF_QUANT_NV
-#define VF_QUANT_NV 2
+#define VF_QUANT_NV 4
 #endif
-constexpr int kNV = VF_QUANT_NV;
+#ifndef VF_DEQUANT_NV
+#define VF_DEQUANT_NV 2
+#endif
+constexpr int kQuantNV = VF_QUANT_NV;
+constexpr int kDequantNV = VF_DEQUANT_NV;
 
 // Multiplier and shift with n / d == (umulhi(n, mul) + n) >> shift for all
 // n < 2^31 and 1 <= d < 2^31 (Granlund and Montgomery's round-up method):
@@ -59,7 +66,7 @@ int pick_vector_width(const Plan &pl) {
 }
 
 // kPath: 0 = generic, one vector per lane; 1 = generic, per-lane loop;
-// 2 = the 8-element path with kNV vectors per lane.
+// 2 = the 8-element path with kQuantNV or kDequantNV vectors per lane.
 template <int VW, int FMT, int kPath>
 int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
     vf::QArgs a;
@@ -99,9 +106,9 @@ int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
         cudaError_t e;
         if constexpr (kPath == 2) {
             if (pl.quantise)
-                e = cudaLaunchKernelEx(&cfg, vf::quantise_rows8<FMT, kNV>, a);
+                e = cudaLaunchKernelEx(&cfg, vf::quantise_rows8<FMT, kQuantNV>, a);
             else
-                e = cudaLaunchKernelEx(&cfg, vf::dequantise_rows8<FMT, kNV>, a);
+                e = cudaLaunchKernelEx(&cfg, vf::dequantise_rows8<FMT, kDequantNV>, a);
         } else {
             if (pl.quantise)
                 e = cudaLaunchKernelEx(&cfg, vf::quantise_rows<VW, FMT, kPath == 0>, a);
@@ -127,8 +134,9 @@ int lanes_log2_for(int64_t nvec, int64_t per_lane) {
 template <int VW, int FMT>
 int launch_vw(const Plan &pl, cudaStream_t stream) {
     const int64_t nvec = pl.D / VW;
-    if (VW == 8 && nvec <= 32 * kNV)
-        return launch_family<VW, FMT, 2>(pl, lanes_log2_for(nvec, kNV), stream);
+    const int64_t nv = pl.quantise ? kQuantNV : kDequantNV;
+    if (VW == 8 && nvec <= 32 * nv)
+        return launch_family<VW, FMT, 2>(pl, lanes_log2_for(nvec, nv), stream);
     const int lg = lanes_log2_for(nvec, 1);
     const bool one = nvec <= (int64_t(1) << lg);
     if (one || !pl.quantise) return launch_family<VW, FMT, 0>(pl, lg, stream);

@@ -12,7 +12,7 @@ signed-zero, below-floor, at-floor and denormal rows (quantising side); valid
 codes (no E4M3 NaN code) with seeded non-negative scales, some zero
 (dequantising side).  Shapes cover every vector width (D % 8, D % 4, D % 2,
 odd strides), a group size that is not a power of two's worth of vectors
-(D = 96), the per-lane loop (D = 512), ragged chunks and shards, empty
+(D = 96), the per-lane loops (D = 520, 1040), ragged chunks and shards, empty
 chunks, chunk ranges, both block orders, pinned host memory, the named C
 entry points, the pages' full workload in full and the large workload on
 sampled rows.
@@ -109,6 +109,9 @@ SHAPES = [
     (77, 4, 12, 4, 5),        # 4-element vectors, empty trailing chunks
     (9, 2, 8, 1, 16),         # more chunks than tokens
     (3, 8, 64, 8, 2),         # fewer tokens than destinations
+    (40, 2, 520, 2, 3),       # 65 vectors: quantise on the 8-element path, the
+                              # dequantiser's per-lane loop
+    (21, 2, 1040, 2, 2),      # 130 vectors: the quantiser's per-lane loop
 ]
 
 
