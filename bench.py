@@ -174,18 +174,43 @@ def calibrate_tokens(cfg, seconds_per_pass: float):
     return tokens, tokens * per_token
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(cfg, budget_s: float = 10.0, cores: int = None):
-    """The oracle on all host cores for about budget_s of wall time."""
+    """The oracle on all host cores for about budget_s of wall time, then on
+    one core (two passes of the same per-core sample)."""
     cores = cores or os.cpu_count() or 1
     tokens, est = calibrate_tokens(cfg, budget_s / 3)
     passes = int(max(3, min(30, budget_s / max(est, 1e-3))))
     per_pass, nbytes = run_oracle(cfg, tokens, passes, cores)
     total = sum(per_pass)
+    one, one_bytes = run_oracle(cfg, tokens, 2, 1)
     return {"value": round(passes * nbytes / total / 1e9, 3), "unit": UNIT, "cores": cores,
             "kind": "oracle",
+            "single_core_value": round(2 * one_bytes / sum(one) / 1e9, 3),
+            "cpu_model": cpu_model(),
             "sample": "%d of %d tokens (H=%d, D=%d, P=%d, C=%d, padded-row pack source, "
                       "head-major split source) per core, one process per core, %d timed "
-                      "passes of pack+split+merge started together, %.1f s"
+                      "passes of pack+split+merge started together, %.1f s; single core: "
+                      "2 passes of the same sample"
                       % (tokens, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, passes, total)}
 
 

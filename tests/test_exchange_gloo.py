@@ -12,7 +12,8 @@ exchanges per chunk, merges, and must hold its token shard with all heads.
 
 The data movement runs in the CPU oracle (no GPU here); what is under test is
 that the [chunk][slot] storage and the piece tables are all a real exchange
-needs.
+needs -- also for the opt-in INT8 transport, whose codes and per-head-row
+scales travel in the same blocks.
 """
 import os
 import socket
@@ -93,7 +94,40 @@ def _rank_main(rank, world, port, shape, out):
             recv_parts.append(_exchange(send, send_sizes, recv_sizes))
         merged = loops.head_merge(torch.cat(recv_parts), b - a, H, D, P, C)
         ret_ok = torch.equal(merged, A[a:b])
-        out[rank] = (bool(fwd_ok), bool(ret_ok))
+
+        # ---- the opt-in lossy transport over the same exchange: INT8 codes and
+        # their per-head-row scales travel in the same blocks (a block of n
+        # elements carries n / D scales); the receiver's dequantised Q, K, V
+        # must equal what the oracle makes of the whole global activation
+        # quantised row by row (the quantiser is per head row, so sharding
+        # cannot change a code)
+        from sequence_head_relayout_gb300 import workloads as W
+        Xf = W.finite_rows_(torch.empty((T, 3, H, D), dtype=torch.int16), 5)
+        codes, scales = loops.qkv_pack_q(Xf[a:b], P, C, loops.INT8)
+        per_tok = 3 * Hp * D
+        rc, rs = [], []
+        for c in range(C):
+            send_sizes = [ptab[1][c * P + p] * per_tok for p in range(P)]
+            recv_sizes = [utab[1][c * P + r] * per_tok for r in range(P)]
+            lo = ptab[2][c * P]
+            send_c = codes[lo:lo + sum(send_sizes)].contiguous()
+            recv_c = torch.empty(sum(recv_sizes), dtype=torch.uint8)
+            dist.all_to_all_single(recv_c, send_c.view(torch.uint8), recv_sizes, send_sizes)
+            rc.append(recv_c)
+            send_s = scales[lo // D:(lo + sum(send_sizes)) // D].contiguous()
+            recv_s = torch.empty(sum(recv_sizes) // D, dtype=torch.float32)
+            dist.all_to_all_single(recv_s, send_s, [n // D for n in recv_sizes],
+                                   [n // D for n in send_sizes])
+            rs.append(recv_s)
+        got = loops.qkv_unpack_q(torch.cat(rc), torch.cat(rs), T, H, D, P, C, loops.INT8)
+        # reference: every head row of the global tensor quantised and
+        # dequantised alone (P = 1, C = 1 split of a [rows, 1, D] view)
+        rows = Xf.view(T * 3 * H, 1, D)
+        c1, s1 = loops.attn_split_q(rows, 1, 1, loops.INT8)
+        ref = loops.head_merge_q(c1, s1, T * 3 * H, 1, D, 1, 1, loops.INT8).view(T, 3, H, D)
+        lossy_ok = all(torch.equal(o, ref[:, s, rank * Hp:(rank + 1) * Hp])
+                       for s, o in enumerate(got))
+        out[rank] = (bool(fwd_ok), bool(ret_ok), bool(lossy_ok))
     finally:
         dist.destroy_process_group()
 
@@ -108,9 +142,9 @@ def _run(world, shape):
 
 def test_two_rank_exchange_round_trips():
     out = _run(2, (37, 8, 16, 4))                 # T odd: short last shard and chunk
-    assert out == {0: (True, True), 1: (True, True)}
+    assert out == {0: (True, True, True), 1: (True, True, True)}
 
 
 def test_two_rank_exchange_pages_like_geometry():
     out = _run(2, (1001, 28, 8, 4))               # pages' H and P, small T and D
-    assert out == {0: (True, True), 1: (True, True)}
+    assert out == {0: (True, True, True), 1: (True, True, True)}
