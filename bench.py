@@ -486,6 +486,7 @@ def gpu_arm(args, rank, world, local_rank):
                                      "head_merge_e4m3")}
         lossy["note"] = ("opt-in INT8 QKV / E4M3 attention-output transport at the bench "
                          "workload; GB/s counts 3 B per element + 4 B per head row")
+        lossy["quality"] = lossy_quality(dev)
     chain_aba = None if args.no_chain else torch_chain_aba(cfg, dev)
 
     line = None
@@ -792,6 +793,40 @@ def torch_chain_aba(cfg, dev, reps=20):
                    "chain_peak_bytes": peak(a_fn), "direct_peak_bytes": peak(b_fn),
                    "outputs_equal": bool(same)}
     return out
+
+
+def lossy_quality(dev, T=4096, H=28, D=128, seed=11):
+    """What the opt-in lossy transport costs in accuracy, on seeded N(0,1)
+    activations at the pages' head count and head dim: the relative L2 error
+    of a causal-free attention output when Q, K and V cross the exchange as
+    INT8 (pack -> unpack, one destination), and of an attention output that
+    crosses as E4M3 (split -> merge)."""
+    import torch
+    import torch.nn.functional as F
+
+    import sequence_head_relayout_gb300 as vf
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    qkv = torch.randn((T, 3, H, D), generator=g, device=dev).to(torch.bfloat16)
+    codes, scales = vf.qkv_pack_q(qkv, 1, 4, fmt="int8")
+    q, k, v = vf.qkv_unpack_q(codes, scales, T, H, D, 1, 4, fmt="int8")
+
+    def sdpa(a, b, c):                      # [T,H,D] -> [1,H,T,D]
+        return F.scaled_dot_product_attention(*(t.permute(1, 0, 2)[None] for t in (a, b, c)))
+
+    ref = sdpa(qkv[:, 0], qkv[:, 1], qkv[:, 2]).float()
+    got = sdpa(q, k, v).float()
+    attn = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    fc, fs = vf.attn_split_q(attn, 1, 4, fmt="e4m3")
+    back = vf.head_merge_q(fc, fs, T, H, D, 1, 4, fmt="e4m3").float()
+
+    def rel(x, y):
+        return float((x - y).norm() / y.norm())
+    qkv_f = qkv.float()
+    return {"shape": "T=%d H=%d D=%d, N(0,1) bf16" % (T, H, D),
+            "int8_qkv_rel_err": round(rel(torch.stack((q, k, v), 1).float(), qkv_f), 6),
+            "int8_qkv_attention_out_rel_err": round(rel(got, ref), 6),
+            "e4m3_attention_out_rel_err": round(rel(back, attn.float()), 6)}
 
 
 def per_config(args, dev):

@@ -364,3 +364,19 @@ def test_large_workload_sampled_rows():
             e = offs[c * P + p] + ((s * L + (t - tok[c * P])) * Hp + hh) * D
             assert torch.equal(cu[e:e + D], wc[i]), (fmt, t, s, h)
             assert int(sc[e // D]) == int(wsb[i]), (fmt, t, s, h)
+
+
+# ------------------------------------------------------------ accuracy gate
+
+def test_transport_accuracy_gate():
+    """The lossy transport's quality gate on seeded N(0,1) activations at the
+    pages' head count and head dim (the benchmark reports the same figures):
+    INT8 Q/K/V through pack -> unpack, then attention; E4M3 attention output
+    through split -> merge.  Expected from the format: INT8 steps are
+    amax/127 (about 0.6% RMS of a unit-variance row), E4M3 keeps 3 mantissa
+    bits (a few % RMS)."""
+    import bench
+    q = bench.lossy_quality(DEV, T=2048)
+    assert 0.002 < q["int8_qkv_rel_err"] < 0.015, q
+    assert 0.0 < q["int8_qkv_attention_out_rel_err"] < 0.02, q
+    assert 0.01 < q["e4m3_attention_out_rel_err"] < 0.05, q
