@@ -1,8 +1,9 @@
 /*
  * Plain C use of the relayout library, without PyTorch: allocate with the
  * CUDA runtime, pack a [T][3][H][D] tensor, unpack it again through the
- * single-rank (P = 1) exchange identity, and compare on the host.  Also
- * checks that a rejected call returns the documented status.  Built and run
+ * single-rank (P = 1) exchange identity, and compare on the host; the same
+ * through the opt-in INT8 and E4M3 transport on exactly quantisable rows.
+ * Also checks that a rejected call returns the documented status.  Built and run
  * by tests/test_gpu_c_driver.py; exits 0 on success.
  */
 #include <stdint.h>
@@ -95,6 +96,64 @@ int main(void) {
         free(h_sm);
         cudaFree(d_cm);
         cudaFree(d_sm);
+    }
+
+    /* the opt-in lossy transport on rows whose quantisation is exact: every
+     * head row holds integers in [-127, 127] with 127 present (INT8: inv = 1,
+     * scale = 1) or E4M3 grid values with 448 present (inv = 1, scale = 1),
+     * so pack -> unpack and split -> merge must reproduce the bf16 bits */
+    {
+        uint16_t *h_x = malloc(n * 2), *h_y = malloc(n * 2);
+        float *h_s = malloc(n / D * sizeof(float));
+        CHECK(h_x && h_y && h_s);
+        static const float grid[8] = {448.0f, -1.0f, 0.5f, 2.0f, -0.015625f, 0.0f, 96.0f, -320.0f};
+        for (int fmt = 0; fmt < 2; ++fmt) {
+            for (int64_t i = 0; i < n; ++i) {
+                float v = fmt == 0 ? (float)((int)((i * 37) % 255) - 127) : grid[(i * 5) % 8];
+                if (i % D == 0) v = fmt == 0 ? 127.0f : 448.0f;
+                uint32_t u;
+                memcpy(&u, &v, 4);
+                h_x[i] = (uint16_t)(u >> 16);          /* exact: few significant bits */
+            }
+            void *d_codes = NULL, *d_scales = NULL;
+            CHECK(cudaMalloc(&d_codes, n) == cudaSuccess);
+            CHECK(cudaMalloc(&d_scales, n / D * sizeof(float)) == cudaSuccess);
+            CHECK(cudaMemcpy(d_src, h_x, n * 2, cudaMemcpyHostToDevice) == cudaSuccess);
+            CHECK(vf_scale_count(VF_OP_QKV_PACK, T, H, D, P, C) == n / D);
+            if (fmt == 0) {
+                CHECK(vf_qkv_pack_int8(d_src, st, T, H, D, P, C, d_codes, d_scales, NULL) == VF_OK);
+                CHECK(vf_qkv_unpack_int8(d_codes, d_scales, T, H, D, P, C, d_q, d_k, d_v, NULL,
+                                         NULL) == VF_OK);
+            } else {
+                /* the [T][3H][D] view of the same buffer as one attention output */
+                const int64_t s3[3] = {3 * H * D, D, 1};
+                CHECK(vf_attn_split_fp8(d_src, s3, T, 3 * H, D, P, C, d_codes, d_scales,
+                                        NULL) == VF_OK);
+                CHECK(vf_head_merge_fp8(d_codes, d_scales, NULL, T, 3 * H, D, P, C, d_packed,
+                                        NULL) == VF_OK);
+            }
+            CHECK(cudaDeviceSynchronize() == cudaSuccess);
+            CHECK(cudaMemcpy(h_s, d_scales, n / D * sizeof(float), cudaMemcpyDeviceToHost) ==
+                  cudaSuccess);
+            for (int64_t r = 0; r < n / D; ++r) CHECK(h_s[r] == 1.0f);
+            if (fmt == 0) {
+                for (int s = 0; s < 3; ++s) {
+                    void *d = s == 0 ? d_q : s == 1 ? d_k : d_v;
+                    CHECK(cudaMemcpy(h_y, d, n * 2 / 3, cudaMemcpyDeviceToHost) == cudaSuccess);
+                    for (int64_t t = 0; t < T; ++t)
+                        for (int64_t x = 0; x < H * D; ++x)
+                            CHECK(h_y[t * H * D + x] == h_x[t * 3 * H * D + s * H * D + x]);
+                }
+            } else {
+                CHECK(cudaMemcpy(h_y, d_packed, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
+                CHECK(memcmp(h_y, h_x, n * 2) == 0);
+            }
+            cudaFree(d_codes);
+            cudaFree(d_scales);
+        }
+        free(h_x);
+        free(h_y);
+        free(h_s);
     }
 
     /* rejected before any launch: H % P != 0 */
