@@ -40,9 +40,9 @@ constexpr int kDequantNV = VF_DEQUANT_NV;
 void fast_divisor(int64_t d, uint32_t *mul, uint32_t *shift) {
     uint32_t l = 0;
     while ((int64_t(1) << l) < d) ++l;
-    const unsigned __int128 num = (static_cast<unsigned __int128>(1) << 32) *
-                                  static_cast<unsigned __int128>((int64_t(1) << l) - d);
-    *mul = uint32_t(num / static_cast<unsigned __int128>(d) + 1);
+    // 2^l - d < d < 2^31, so the numerator is below 2^63
+    const uint64_t num = uint64_t((int64_t(1) << l) - d) << 32;
+    *mul = uint32_t(num / uint64_t(d) + 1);
     *shift = l;
 }
 
