@@ -296,3 +296,82 @@ def test_bad_format_is_rejected():
     x = _bf16_bits(torch.ones(2, 1, 8))
     with pytest.raises(Exception):
         loops.attn_split_q(x, 1, 1, 3)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _mutant_split_codes(x_bits, fmt, kind):
+    """A restated per-head-row quantiser with one planted mistake (kind), on a
+    [T,H,D] bf16 view with P = C = 1 (the split's layout is then the identity).
+    Returns (codes as int list, scales as float list)."""
+    import numpy as np
+    x = _bits_to_f32(x_bits.contiguous()).numpy().astype(np.float32)
+    T, H, D = x.shape
+    top = np.float32(127.0 if fmt == INT8 else 448.0)
+    if kind == "per_token_amax":
+        amax = np.abs(x).reshape(T, H * D).max(axis=1).repeat(H).reshape(T, H, 1)
+    else:
+        amax = np.abs(x).max(axis=2, keepdims=True)
+    live = amax >= np.float32(2.0 ** -96) if kind != "no_floor" else amax > 0
+    if kind == "scale_128":
+        top_q = np.float32(128.0)
+    else:
+        top_q = top
+    with np.errstate(divide="ignore", invalid="ignore"):
+        inv = np.where(live, top_q / amax, np.float32(0)).astype(np.float32)
+        scale = np.where(live, amax / top, np.float32(0)).astype(np.float32)
+    q = (x * inv).astype(np.float32)
+    if fmt == INT8:
+        if kind == "truncate":
+            r = np.trunc(q)
+        elif kind == "half_away":
+            r = np.sign(q) * np.floor(np.abs(q) + np.float32(0.5))
+        else:
+            r = np.rint(q)
+        c = np.clip(r, -127, 127).astype(np.int64)
+        c = np.where(live, c, 0)
+        codes = [int(v) for v in c.reshape(-1)]
+    else:
+        t = torch.from_numpy(q.reshape(-1))
+        if kind == "truncate":                  # round toward zero onto the E4M3 grid
+            rn = t.clamp(-448, 448).to(torch.float8_e4m3fn).float()
+            over = rn.abs() > t.abs()
+            # step back one code where rounding went away from zero
+            cb = rn.to(torch.float8_e4m3fn).view(torch.uint8).to(torch.int32)
+            cb = torch.where(over & (cb & 0x7F > 0), cb - 1, cb)
+            cc = cb
+        else:
+            cc = t.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).to(torch.int32)
+        cc = torch.where(torch.from_numpy(np.broadcast_to(live, q.shape).reshape(-1).copy()),
+                         cc, torch.zeros_like(cc))
+        codes = [int(v) for v in cc]
+    return codes, [float(v) for v in scale.reshape(-1)]
+
+
+def _pin_inputs():
+    """The pinned rows: the hand row, the INT8 ties row, exact-grid rows with
+    per-row exponents, a below-floor row (as [T,H,D] bf16 bits)."""
+    hand = _bf16_bits(torch.tensor([1.0, -0.5, 0.25, 0.0, 0.75, -1.0, 0.125, 0.375])).view(1, 1, 8)
+    ties = _bf16_bits(torch.tensor([127.0, 0.5, 1.5, 2.5, -0.5, -2.5, 3.5, 126.5])).view(1, 1, 8)
+    floor = _bf16_bits(torch.tensor([1e-30, -2e-30, 0, 0, 0, 0, 0, 3e-31])).view(1, 1, 8)
+    return [hand, ties, floor] + [_grid_rows((5, 4, 8), f, 900 + f)[0] for f in (INT8, E4M3)]
+
+
+@pytest.mark.parametrize("kind", ["truncate", "half_away", "scale_128", "per_token_amax",
+                                  "no_floor"])
+@pytest.mark.parametrize("fmt", [INT8, E4M3])
+def test_pins_catch_planted_lossy_mistakes(kind, fmt):
+    """The unmutated restatement reproduces the oracle on every pinned input;
+    each planted mistake changes a code or a scale on at least one of them
+    (half-away rounding does not exist for the E4M3 encoder, which the
+    library conversion decides; that case checks INT8 only)."""
+    if fmt == E4M3 and kind == "half_away":
+        pytest.skip("E4M3 rounding is pinned against PyTorch's conversion directly")
+    caught = False
+    for x in _pin_inputs():
+        c_ok, s_ok = loops.attn_split_q(x, 1, 1, fmt)
+        want = ([int(v) for v in c_ok.tolist()] if fmt == INT8 else
+                [int(v) for v in c_ok.view(torch.uint8).tolist()], s_ok.tolist())
+        assert _mutant_split_codes(x, fmt, "none") == want
+        caught = caught or _mutant_split_codes(x, fmt, kind) != want
+    assert caught, kind
