@@ -112,6 +112,7 @@ SHAPES = [
     (40, 2, 520, 2, 3),       # 65 vectors: quantise on the 8-element path, the
                               # dequantiser's per-lane loop
     (21, 2, 1040, 2, 2),      # 130 vectors: the quantiser's per-lane loop
+    (100, 64, 8, 64, 64),     # 12,288 pack pieces: many launches of 120
 ]
 
 

@@ -111,6 +111,8 @@ EDGE_SHAPES = [
     (5, 4, 4096, 2, 2),     # long head rows: one block row spans 512 vectors
     (3, 2, 8192, 2, 1),     # head rows longer than one block: d chunks
     (7, 1024, 8, 2, 2),     # many heads per row: head chunks
+    (100, 64, 8, 64, 64),   # P * C = 4096 blocks: 96 pack launches, mostly empty shards
+    (2, 8, 8, 8, 131072),   # P * C = 2^20, the table limit: all but two chunks empty
 ]
 
 
