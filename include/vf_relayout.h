@@ -292,7 +292,9 @@ int64_t vf_piece_table_ex(int op, int order, int64_t T, int64_t H, int64_t D, in
  *     E4M3: code = q as OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7,
  *           3 mantissa bits), saturating at +-448, never NaN.
  *   Receive side: y = bfloat16(value(code) * scale).
- * Inputs must be finite (NaN or infinity gives unspecified codes).
+ * The 16-bit elements are BF16 values on both sides (the quantisers read
+ * them as BF16, the dequantisers write BF16).  Inputs must be finite (NaN or
+ * infinity gives unspecified codes).
  *
  * Storage: codes: one byte per element, in exactly the element layout of
  * the exact op (vf_packed_elems bytes; block offsets are vf_piece_table's

@@ -417,11 +417,19 @@ def _rows(n, D):
     return n // D if D > 0 else 0
 
 
+def _check_bf16(t: torch.Tensor, what: str):
+    """The lossy transport reads and writes BF16 values (int16 views of BF16
+    bit patterns are accepted too); float16 would be misread."""
+    if isinstance(t, torch.Tensor) and t.dtype not in (torch.bfloat16, torch.int16):
+        raise ValueError("%s must hold bfloat16 values (or their int16 bit patterns)" % what)
+    _check16(t, what)
+
+
 def qkv_pack_q(src: torch.Tensor, P: int, C: int, fmt="int8", codes=None, scales=None,
                stream: torch.cuda.Stream = None, chunks=None, order="chunk_major"):
     """Quantising QKV pack of a [T,3,H,D] bf16 view -> (codes, scales): the
     layout of :func:`qkv_pack`, one byte per element, one scale per head row."""
-    _check16(src, "src")
+    _check_bf16(src, "src")
     if src.dim() != 4 or src.shape[1] != 3:
         raise ValueError("src must be a [T,3,H,D] view")
     f = _fmt(fmt)
@@ -438,7 +446,7 @@ def qkv_pack_q(src: torch.Tensor, P: int, C: int, fmt="int8", codes=None, scales
 def attn_split_q(src: torch.Tensor, P: int, C: int, fmt="e4m3", codes=None, scales=None,
                  stream: torch.cuda.Stream = None, chunks=None, order="chunk_major"):
     """Quantising attention-result split of a [T,H,D] bf16 view -> (codes, scales)."""
-    _check16(src, "src")
+    _check_bf16(src, "src")
     if src.dim() != 3:
         raise ValueError("src must be a [T,H,D] view")
     f = _fmt(fmt)
@@ -461,7 +469,7 @@ def head_merge_q(codes: torch.Tensor, scales: torch.Tensor, T: int, H: int, D: i
     if out is None:
         out = torch.empty((T, H, D), dtype=torch.bfloat16, device=codes.device,
                           pin_memory=codes.device.type == "cpu")
-    _check16(out, "out")
+    _check_bf16(out, "out")
     if tuple(out.shape) != (T, H, D):
         raise ValueError("out must have shape [T,H,D]")
     _relayout(OP_HEAD_MERGE, _order(order), T, H, D, P, C, chunks, codes.data_ptr(),
@@ -483,7 +491,7 @@ def qkv_unpack_q(codes: torch.Tensor, scales: torch.Tensor, T: int, H: int, D: i
                                  pin_memory=codes.device.type == "cpu") for _ in range(3))
     q, k, v = outs
     for t, name in ((q, "q"), (k, "k"), (v, "v")):
-        _check16(t, name)
+        _check_bf16(t, name)
         if tuple(t.shape) != (T, Hp, D):
             raise ValueError("%s must have shape [T,H/P,D]" % name)
     if q.stride() != k.stride() or q.stride() != v.stride():

@@ -96,3 +96,7 @@ def test_binding_refuses_pageable_and_bad_formats(L):
         vf.attn_split_q(x, 2, 1)
     with pytest.raises(ValueError):
         vf.qkv_pack_q(torch.zeros((4, 3, 2, 8), dtype=torch.bfloat16), 2, 1, fmt="fp4")
+    # float16 would be read as bfloat16 bit patterns: refused for its dtype
+    # (checked before the memory kind)
+    with pytest.raises(ValueError, match="bfloat16"):
+        vf.attn_split_q(torch.zeros((4, 2, 8), dtype=torch.float16), 2, 1)
