@@ -304,8 +304,10 @@ int64_t vf_piece_table_ex(int op, int order, int64_t T, int64_t H, int64_t D, in
  * other or the strided views.  Codes may be at any address; the kernels use
  * 8-element vectors when D % 8 == 0, the strided side is 16-byte aligned
  * with d contiguous, and codes are 8-byte aligned.
- * Additional limit: tokens x heads of any one (chunk, destination) block
- * below 2^31, else VF_ERR_ARG.
+ * Errors as for the exact calls, plus: an unknown format, NULL scales (when
+ * anything is moved) or scales not 4-byte aligned -> VF_ERR_ARG; scales that
+ * overlap the codes or a strided view -> VF_ERR_ALIAS; tokens x heads of any
+ * one (chunk, destination) block at or above 2^31 -> VF_ERR_ARG.
  */
 typedef enum vf_format {
     VF_FORMAT_INT8 = 1,

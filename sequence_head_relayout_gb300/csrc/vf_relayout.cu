@@ -278,6 +278,7 @@ int run(Request rq, cudaStream_t stream) {
         int64_t rows;
     };
     std::vector<Raw> raw;
+    raw.reserve(size_t((rq.c_end - rq.c_begin) * s.P * slabs));
     for (int64_t c = rq.c_begin; c < rq.c_end; ++c)
         for (int64_t p = 0; p < s.P; ++p) {
             const Entry &e = table[size_t(c * s.P + p)];
