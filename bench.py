@@ -194,6 +194,44 @@ def cpu_model() -> str:
     return platform.machine()
 
 
+def lossy_cpu_baseline(cfg, tokens: int = 2048, passes: int = 2):
+    """The lossy-transport oracle on one host core, on a token sample of the
+    workload: GB/s per op with the lossy byte count (3 B per element + 4 B
+    per head row), best of `passes`."""
+    import torch
+
+    from oracle import loops
+    from sequence_head_relayout_gb300 import workloads as W
+    T, H, D, P, C = min(tokens, cfg.T), cfg.H, cfg.D, cfg.P, cfg.C
+    x4 = W.finite_rows_(torch.empty((T, 3, H, D), dtype=torch.int16), 1)
+    x3 = W.finite_rows_(torch.empty((T, H, D), dtype=torch.int16), 2)
+    ops = {}
+
+    def timed(name, elems, fn):
+        best = min(_wall(fn) for _ in range(passes))
+        ops[name] = round(lossy_bytes(elems, D) / best / 1e9, 3)
+
+    codes, scales = loops.qkv_pack_q(x4, P, C, loops.INT8)
+    fcodes, fscales = loops.attn_split_q(x3, P, C, loops.E4M3)
+    n_unpack = 3 * T * (H // P) * D
+    timed("qkv_pack_int8", 3 * T * H * D, lambda: loops.qkv_pack_q(x4, P, C, loops.INT8))
+    timed("qkv_unpack_int8", n_unpack, lambda: loops.qkv_unpack_q(
+        codes[:n_unpack], scales[:n_unpack // D], T, H, D, P, C, loops.INT8))
+    timed("attn_split_e4m3", T * H * D, lambda: loops.attn_split_q(x3, P, C, loops.E4M3))
+    timed("head_merge_e4m3", T * H * D, lambda: loops.head_merge_q(
+        fcodes, fscales, T, H, D, P, C, loops.E4M3))
+    return {"unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d of %d tokens (H=%d, D=%d, P=%d, C=%d), finite bf16 rows, best of %d"
+                      % (T, cfg.T, H, D, P, C, passes),
+            "ops": ops}
+
+
+def _wall(fn) -> float:
+    t0 = time.perf_counter()
+    fn()
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(cfg, budget_s: float = 10.0, cores: int = None):
     """The oracle on all host cores for about budget_s of wall time, then on
     one core (two passes of the same per-core sample)."""
@@ -1008,6 +1046,8 @@ def main():
             from sequence_head_relayout_gb300 import workloads as W
             line["cpu_baseline"] = cpu_baseline(W.CONFIGS[args.config],
                                                 cores=args.cpu_cores or None)
+            line["cpu_baseline"]["lossy_single_core"] = lossy_cpu_baseline(
+                W.CONFIGS[args.config])
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)
