@@ -45,3 +45,43 @@ def test_threads_on_separate_streams():
     assert not errors, errors
     for (x, _, P, C), got in zip(jobs, results):
         assert torch.equal(got.cpu(), loops.qkv_pack(x, P, C))
+
+
+def test_lossy_threads_on_separate_streams():
+    """The same for the opt-in lossy transport: concurrent quantising packs
+    (INT8) and splits (E4M3) from eight host threads."""
+    from sequence_head_relayout_gb300 import workloads as W
+    shapes = [(777 + 53 * i, 8, 128, (2, 4, 8)[i % 3], 1 + i % 4) for i in range(8)]
+    jobs = []
+    for i, (T, H, D, P, C) in enumerate(shapes):
+        x4 = W.finite_rows_(torch.empty((T, 3, H, D), dtype=torch.int16), 100 + i)
+        x3 = W.finite_rows_(torch.empty((T, H, D), dtype=torch.int16), 200 + i)
+        jobs.append((x4, x3, x4.to(DEV), x3.to(DEV), P, C))
+    torch.cuda.synchronize()
+    results = [None] * len(jobs)
+    errors = []
+
+    def work(i):
+        try:
+            _, _, x4d, x3d, P, C = jobs[i]
+            s = torch.cuda.Stream(DEV)
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    packed = vf.qkv_pack_q(x4d, P, C, fmt="int8")
+                    split = vf.attn_split_q(x3d, P, C, fmt="e4m3")
+                results[i] = (packed, split)
+            s.synchronize()
+        except Exception as e:            # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (x4, x3, _, _, P, C), ((pc, ps), (sc, ss)) in zip(jobs, results):
+        wc, ws = loops.qkv_pack_q(x4, P, C, loops.INT8)
+        assert torch.equal(pc.cpu(), wc) and torch.equal(ps.cpu(), ws)
+        wc, ws = loops.attn_split_q(x3, P, C, loops.E4M3)
+        assert torch.equal(sc.cpu().view(torch.uint8), wc) and torch.equal(ss.cpu(), ws)
