@@ -15,7 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "vf_relayout.cu"), os.path.join(CSRC, "vf_quant.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, n) for n in ("relayout_kernel.cuh", "launch.cuh",
-                                                  "quant_kernel.cuh", "quant.h")] \
+                                                  "tiled_kernel.cuh", "quant_kernel.cuh",
+                                                  "quant.h")] \
     + [os.path.join(ROOT, "include", "vf_relayout.h")]
 LIB = os.path.join(PKG, "libvf_relayout.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

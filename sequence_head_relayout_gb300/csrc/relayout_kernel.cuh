@@ -13,11 +13,13 @@
 //             + row * row_stride + head * head_stride + d * d_stride.
 //
 // There is no element-level transpose: the (token, head) interchange between
-// the two sides happens at the granularity of whole D-element head rows (at
-// least 32 B, one DRAM sector, for every shape accepted on the vector paths),
-// so both sides stay sector-complete with plain 16-byte loads and stores and
-// no shared-memory staging.  The block is a 3-D thread array
-// (x: VW-element vector within a head row, y: head, z: row) so the address of
+// the two sides happens at the granularity of whole D-element head rows (256 B
+// at D = 128; at least one 32-byte DRAM sector from D = 16 up), so both sides
+// stay sector-complete with plain 16-byte loads and stores and no
+// shared-memory staging.  (Shorter head rows on a head-major strided side go
+// through the shared-memory tile of tiled_kernel.cuh instead.)  The block is a
+// 3-D thread array (x: VW-element vector within a head row, y: head, z: row)
+// so the address of
 // a thread is a sum of products (the only divisions are block-uniform), and a
 // warp covers consecutive packed vectors.  Each thread keeps kRowsPerThread
 // independent loads in flight before it stores.  Offsets are 64-bit

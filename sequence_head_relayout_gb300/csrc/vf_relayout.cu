@@ -21,6 +21,7 @@
 
 #include "quant.h"
 #include "relayout_kernel.cuh"
+#include "tiled_kernel.cuh"
 #include "vf_relayout.h"
 
 namespace {
@@ -200,6 +201,83 @@ struct Request {
 // Block shape, vector width, grid order and launches.
 #include "launch.cuh"
 
+// The shared-memory staged path (tiled_kernel.cuh): 16- or 32-byte head rows
+// (D = 8 or 16), unit d-stride, a head-major strided side (consecutive tokens
+// of one head closer together than consecutive heads of one token), every
+// head row 16-byte aligned.
+#ifndef VF_TILED_MAX_D
+#define VF_TILED_MAX_D 16
+#endif
+bool use_tiled(const Plan &pl) {
+    if (pl.d_stride != 1 || pl.heads < 2) return false;
+    if (pl.D > VF_TILED_MAX_D || (pl.D != 8 && pl.D != 16 && pl.D != 32 && pl.D != 64 &&
+                                  pl.D != 128)) return false;
+    if (pl.row_stride >= pl.head_stride) return false;
+    if (pl.row_stride % 8 || pl.head_stride % 8) return false;
+    if (ceil_div(pl.heads, vf::kTileHeads) > kMaxGridZ) return false;
+    if (reinterpret_cast<uintptr_t>(pl.packed) % 16) return false;
+    for (const auto &p : pl.pieces)
+        if (reinterpret_cast<uintptr_t>(p.strided) % 16) return false;
+    return true;
+}
+
+template <int DV, bool kPackedIsDst>
+int launch_tiled(const Plan &pl, cudaStream_t stream) {
+    vf::TiledArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.packed = pl.packed;
+    a.row_stride = pl.row_stride;
+    a.head_stride = pl.head_stride;
+    a.heads = int32_t(pl.heads);
+    a.head_tiles = int32_t(ceil_div(pl.heads, vf::kTileHeads));
+    const size_t n = pl.pieces.size();
+    for (size_t first = 0; first < n; first += vf::kMaxPieces) {
+        const size_t cnt = std::min<size_t>(vf::kMaxPieces, n - first);
+        int64_t max_rows = 0;
+        for (size_t i = 0; i < cnt; ++i) {
+            a.pieces[i] = pl.pieces[first + i];
+            max_rows = std::max(max_rows, a.pieces[i].rows);
+        }
+        if (max_rows == 0) continue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(ceil_div(max_rows, vf::TileShape<DV>::kTok)), unsigned(cnt),
+                           unsigned(a.head_tiles));
+        cfg.blockDim = dim3(unsigned(vf::kTileThreads), 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+#if VF_PDL
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+#endif
+        if (cudaLaunchKernelEx(&cfg, vf::relayout_tiled<DV, kPackedIsDst>, a) != cudaSuccess) {
+            cudaGetLastError();
+            return VF_ERR_CUDA;
+        }
+    }
+    return VF_OK;
+}
+
+template <bool kPackedIsDst>
+int launch_tiled_dir(const Plan &pl, cudaStream_t stream) {
+    switch (pl.D) {
+        case 8: return launch_tiled<1, kPackedIsDst>(pl, stream);
+        case 16: return launch_tiled<2, kPackedIsDst>(pl, stream);
+#if VF_TILED_MAX_D >= 32
+        case 32: return launch_tiled<4, kPackedIsDst>(pl, stream);
+#endif
+#if VF_TILED_MAX_D >= 64
+        case 64: return launch_tiled<8, kPackedIsDst>(pl, stream);
+#endif
+#if VF_TILED_MAX_D >= 128
+        case 128: return launch_tiled<16, kPackedIsDst>(pl, stream);
+#endif
+        default: return VF_ERR_ARG;
+    }
+}
+
 int run(Request rq, cudaStream_t stream) {
     const Shape &s = rq.s;
     int rc = check_shape(s);
@@ -320,6 +398,9 @@ int run(Request rq, cudaStream_t stream) {
     pl.D = s.D;
     pl.piece_fastest = schedule_pieces_first(s.op);
     for (const Raw &r : raw) pl.pieces.push_back({r.packed_off, r.base, r.rows});
+    if (use_tiled(pl))
+        return packed_is_dst ? launch_tiled_dir<true>(pl, stream)
+                             : launch_tiled_dir<false>(pl, stream);
     const int vw = pick_vector_width(pl);
     return packed_is_dst ? launch_dir<true>(pl, vw, stream) : launch_dir<false>(pl, vw, stream);
 }
