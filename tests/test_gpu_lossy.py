@@ -381,3 +381,41 @@ def test_transport_accuracy_gate():
     assert 0.002 < q["int8_qkv_rel_err"] < 0.015, q
     assert 0.0 < q["int8_qkv_attention_out_rel_err"] < 0.02, q
     assert 0.01 < q["e4m3_attention_out_rel_err"] < 0.05, q
+
+
+# ------------------------------------------------------------ rounding ties on the device
+
+def _e4m3_positive_grid():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).float()
+    return sorted({v for v in vals.tolist() if v == v and v >= 0})
+
+
+@pytest.mark.parametrize("fmt", ["int8", "e4m3"])
+def test_rounding_ties_on_device(fmt):
+    """Rows whose scale factor is exactly 1 (amax = 127 or 448), so that
+    q = x: every half-integer (INT8) and every midpoint between neighbouring
+    E4M3 values (all exact in bfloat16) is a tie, which the device must round
+    to even exactly as the oracle does; both signs, on both vector paths."""
+    if fmt == "int8":
+        top = 127.0
+        ties = [k + 0.5 for k in range(0, 127)]
+    else:
+        top = 448.0
+        grid = _e4m3_positive_grid()
+        ties = [(a + b) / 2 for a, b in zip(grid, grid[1:])]
+    vals = ties + [-t for t in ties]
+    D = 128
+    rows = -(-len(vals) // (D - 1))
+    x = torch.zeros(rows, D)
+    flat = torch.tensor(vals + [0.0] * (rows * (D - 1) - len(vals)))
+    x[:, 1:] = flat.view(rows, D - 1)
+    x[:, 0] = top
+    xb = x.to(torch.bfloat16)
+    assert torch.equal(xb.float(), x)                      # every tie exact in bfloat16
+    bits = xb.view(torch.int16).view(rows, 1, D)
+    for D_used, sl in ((D, bits), (6, bits[:, :, :6].contiguous())):
+        codes, scales = vf.attn_split_q(sl.to(DEV), 1, 1, fmt=fmt)
+        wc, ws = loops.attn_split_q(sl, 1, 1, FMT[fmt])
+        assert torch.equal(u8(codes), u8(wc)), first_diff(u8(codes), u8(wc))
+        assert torch.equal(i32(scales), i32(ws))
