@@ -390,8 +390,16 @@ int64_t oracle_reorder_blocks(int op, int64_t T, int64_t H, int64_t D, int64_t P
  * not depend on whether denormals are flushed.  Codes use the element layout
  * of the exact ops (one byte per element); scales are one float per head row
  * in the order of the rows in that layout (scale index = element offset / D).
- * Inputs must be finite.  rintf() uses the default rounding mode (nearest,
- * ties to even).
+ * Non-finite values (the pages give no format, so this is the build's
+ * reading too): a head row holding a NaN or an infinity has no scale that
+ * represents it, so it is sent as a lost row -- scale = the float32 quiet NaN
+ * 0x7FC00000 and every code 0 -- and never disturbs another row.  The
+ * receive side writes the bfloat16 quiet NaN 0x7FC0 into every element of a
+ * row whose scale is not finite (NaN or an infinity), so a lost row arrives
+ * as NaN and never as a plausible value.  The E4M3 codes 0x7F and 0xFF (the
+ * format's NaN) are never written; their value is NaN, and a receive side
+ * given one writes a NaN there.
+ * rintf() uses the default rounding mode (nearest, ties to even).
  */
 
 static float bf16_to_f32(uint16_t b) {
@@ -437,6 +445,7 @@ static uint8_t e4m3_encode(float f) {
 static float e4m3_decode(uint8_t c) {
     float sign = (c & 0x80) ? -1.0f : 1.0f;
     int exp = (c >> 3) & 0xF, m = c & 7;
+    if (exp == 15 && m == 7) return NAN;                      /* 0x7F, 0xFF */
     if (exp == 0) return sign * ldexpf((float)m, -9);
     return sign * ldexpf(1.0f + (float)m / 8.0f, exp - 7);
 }
@@ -447,9 +456,17 @@ static int bad_fmt(int fmt) { return fmt != 1 && fmt != 2; }
 static void quantise_row(const uint16_t *x, int64_t ds, int64_t D, int fmt,
                          uint8_t *codes, float *scale) {
     float amax = 0.0f;
+    int finite = 1;
     for (int64_t d = 0; d < D; ++d) {
         float v = fabsf(bf16_to_f32(x[d * ds]));
-        if (v > amax) amax = v;
+        if (!isfinite(v)) finite = 0;
+        else if (v > amax) amax = v;
+    }
+    if (!finite) {                                  /* a lost row: NaN scale, zero codes */
+        const uint32_t qnan = 0x7FC00000u;
+        memcpy(scale, &qnan, 4);
+        for (int64_t d = 0; d < D; ++d) codes[d] = 0;
+        return;
     }
     const float top = fmt == 2 ? 448.0f : 127.0f;
     const int live = amax >= 0x1p-96f;
@@ -471,8 +488,10 @@ static void quantise_row(const uint16_t *x, int64_t ds, int64_t D, int fmt,
 }
 
 static uint16_t dequantise(uint8_t code, float scale, int fmt) {
+    if (!isfinite(scale)) return 0x7FC0;            /* a lost row */
     const float v = fmt == 2 ? e4m3_decode(code) : (float)(int8_t)code;
-    return f32_to_bf16(v * scale);
+    if (isnan(v)) return 0x7FC0;                    /* an E4M3 NaN code */
+    return f32_to_bf16(v * scale);                  /* finite, or an overflow to +-inf */
 }
 
 /* Quantising QKV pack: the pack's loop nest, one head row at a time. */

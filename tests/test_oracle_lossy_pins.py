@@ -44,7 +44,8 @@ def test_e4m3_decode_every_code_matches_torch():
     codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
     ref = codes.view(torch.float8_e4m3fn).float()
     for c in range(256):
-        if c in (0x7F, 0xFF):                # the two NaN codes are never produced
+        if c in (0x7F, 0xFF):                # the format's two NaN codes (never written)
+            assert math.isnan(loops.e4m3_decode(c)) and math.isnan(ref[c].item())
             continue
         assert loops.e4m3_decode(c) == ref[c].item(), hex(c)
 
@@ -290,6 +291,104 @@ def test_signed_zero_in_a_live_row():
     assert (cf.to(torch.int32) & 0xFF).tolist() == [0x80, 0x7E, 0x00, 0xFE]
     y = loops.head_merge_q(cf, sf, 1, 1, 4, 1, 1, E4M3)
     assert (y.to(torch.int32) & 0xFFFF).flatten().tolist() == [0x8000, 0x3F80, 0x0000, 0xBF80]
+
+
+# ---------------------------------------------------------------- non-finite rows
+#
+# Reading of the variant for values the pages' format cannot carry: a head
+# row holding a NaN or an infinity is sent as a lost row (scale = the float32
+# quiet NaN 0x7FC00000, every code 0); the receive side writes the bfloat16
+# quiet NaN 0x7FC0 into every element of a row whose scale is not finite.
+
+QNAN32, QNAN16 = 0x7FC00000, 0x7FC0
+HAND_BITS = [0x3F80, 0xBF00, 0x3E80, 0x0000, 0x3F40, 0xBF80, 0x3E00, 0x3EC0]   # the hand row
+
+
+def _u32(t: torch.Tensor):
+    return [v & 0xFFFFFFFF for v in t.contiguous().view(torch.int32).tolist()]
+
+
+def _u16(t: torch.Tensor):
+    return [v & 0xFFFF for v in t.contiguous().view(torch.int16).flatten().tolist()]
+
+
+def _as_i16(rows):
+    return torch.tensor([[v - 0x10000 if v >= 0x8000 else v for v in r] for r in rows],
+                        dtype=torch.int16)
+
+
+@pytest.mark.parametrize("fmt", [INT8, E4M3])
+def test_nonfinite_rows_are_sent_as_lost_rows(fmt):
+    rows = [[0x3F80, 0x7FC0, 0x4000, 0, 0, 0, 0, 0],          # 1, quiet NaN, 2
+            [0x3F80, 0x7F80, 0x4000, 0, 0, 0, 0, 0],          # +inf beside finite values
+            [0xFF80, 0, 0, 0, 0, 0, 0, 0],                    # -inf alone
+            [0, 0, 0, 0, 0, 0, 0, 0xFFC1],                    # a negative NaN with payload
+            [0x7F81, 0x7F80, 0xFF80, 0x7FC0, 0, 0, 0, 0],     # several kinds at once
+            HAND_BITS]                                        # finite: as if it were alone
+    x = _as_i16(rows).view(len(rows), 1, 8)
+    codes, scales = loops.attn_split_q(x, 1, 1, fmt)
+    assert _u32(scales)[:5] == [QNAN32] * 5
+    assert [v & 0xFF for v in codes[:40].view(torch.int8).tolist()] == [0] * 40
+    hand_c, hand_s = loops.attn_split_q(_as_i16([HAND_BITS]).view(1, 1, 8), 1, 1, fmt)
+    assert torch.equal(codes[40:].view(torch.int8), hand_c.view(torch.int8))
+    assert _u32(scales[5:]) == _u32(hand_s)
+    # the receive side: lost rows arrive as NaN, the finite row unchanged
+    y = loops.head_merge_q(codes, scales, len(rows), 1, 8, 1, 1, fmt)
+    assert _u16(y)[:40] == [QNAN16] * 40
+    assert _u16(y[5:]) == _u16(loops.head_merge_q(hand_c, hand_s, 1, 1, 8, 1, 1, fmt))
+
+
+@pytest.mark.parametrize("fmt", [INT8, E4M3])
+def test_non_finite_scales_dequantise_to_nan_rows(fmt):
+    # codes 1, -1, 0, full scale, ... under scales +inf, -inf, a NaN with a
+    # payload and the sign set, and 2^127 (finite; its products overflow)
+    full = 127 if fmt == INT8 else 0x7E                       # 127 or 448
+    one = 1 if fmt == INT8 else 0x38                          # 1.0
+    neg_full = (-127) & 0xFF if fmt == INT8 else 0xFE
+    c = torch.tensor([one, full, 0, neg_full] * 4, dtype=torch.uint8)
+    s = torch.tensor([0x7F800000, 0xFF800000, 0xFFC00001, 0x7F000000],
+                     dtype=torch.int64).to(torch.int32).view(torch.float32)
+    if fmt == INT8:
+        c = c.view(torch.int8)
+    y = _u16(loops.head_merge_q(c, s, 4, 1, 4, 1, 1, fmt))
+    assert y[:12] == [QNAN16] * 12
+    # 1 * 2^127 = 0x7F00 in bfloat16; 127 * 2^127 and 448 * 2^127 overflow
+    # float32 and round to +inf (0x7F80); 0 stays +0; the negative full scale
+    # goes to -inf (0xFF80)
+    assert y[12:] == [0x7F00, 0x7F80, 0x0000, 0xFF80]
+
+
+def test_e4m3_nan_codes_dequantise_to_nan():
+    c = torch.tensor([0x7F, 0xFF, 0x38, 0xB8], dtype=torch.uint8)
+    s = torch.tensor([1.0], dtype=torch.float32)
+    y = loops.head_merge_q(c, s, 1, 1, 4, 1, 1, E4M3)
+    v = y.view(torch.bfloat16).float().flatten()
+    assert math.isnan(v[0].item()) and math.isnan(v[1].item())
+    assert v[2:].tolist() == [1.0, -1.0]
+
+
+@pytest.mark.parametrize("fmt", [INT8, E4M3])
+def test_lost_rows_leave_the_other_rows_alone(fmt):
+    # planting NaN or infinity into some rows changes exactly those rows'
+    # codes and scales; every other row is what it was without them
+    T, H, D = 24, 5, 16
+    xb = _random_rows(T, H, D, 31).clone()
+    ref_c, ref_s = loops.attn_split_q(xb, 2, 3, fmt)
+    g = torch.Generator().manual_seed(32)
+    lost = torch.zeros(T, H, dtype=torch.bool)
+    for i in range(12):
+        t, h, d = (int(torch.randint(0, n, (1,), generator=g)) for n in (T, H, D))
+        xb[t, h, d] = (0x7FC0, 0x7F80, -0x80, -0x3F)[i % 4]    # NaN, +inf, -inf, NaN 0xFFC1
+        lost[t, h] = True
+    c, s = loops.attn_split_q(xb, 2, 3, fmt)
+    # the split's layout of the lost-row mask (as 16-bit ones), one per head row
+    mask = loops.attn_split(lost.to(torch.int16).unsqueeze(-1).expand(T, H, D).contiguous(),
+                            2, 3)[::D].bool()
+    assert int(mask.sum()) == int(lost.sum())
+    sb, rb = torch.tensor(_u32(s)), torch.tensor(_u32(ref_s))
+    assert bool((sb[mask] == QNAN32).all()) and torch.equal(sb[~mask], rb[~mask])
+    cc, rc = c.view(torch.uint8).view(-1, D), ref_c.view(torch.uint8).view(-1, D)
+    assert int(cc[mask].sum()) == 0 and torch.equal(cc[~mask], rc[~mask])
 
 
 def test_bad_format_is_rejected():
