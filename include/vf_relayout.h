@@ -293,8 +293,15 @@ int64_t vf_piece_table_ex(int op, int order, int64_t T, int64_t H, int64_t D, in
  *           3 mantissa bits), saturating at +-448, never NaN.
  *   Receive side: y = bfloat16(value(code) * scale).
  * The 16-bit elements are BF16 values on both sides (the quantisers read
- * them as BF16, the dequantisers write BF16).  Inputs must be finite (NaN or
- * infinity gives unspecified codes).
+ * them as BF16, the dequantisers write BF16).
+ * Non-finite values: a head row holding a NaN or an infinity cannot be
+ * scaled, so it is sent as a lost row: scale = the float32 quiet NaN
+ * 0x7FC00000 and every code 0; no other row is affected.  The receive side
+ * writes the BF16 quiet NaN 0x7FC0 into every element of a row whose scale
+ * is not finite (NaN or an infinity).  The E4M3 codes 0x7F and 0xFF (the
+ * format's NaN) are never written; a receive side given one writes a NaN
+ * there (payload unspecified).  A finite product that overflows float32
+ * arrives as an infinity.
  *
  * Storage: codes: one byte per element, in exactly the element layout of
  * the exact op (vf_packed_elems bytes; block offsets are vf_piece_table's

@@ -14,6 +14,10 @@
 // clamp(round_half_even(q), +-127) for INT8 or the nearest E4M3 value (ties
 // to even, saturating at +-448).  Dequantisation: bf16(value(code) * scale),
 // the product rounded to float32 and then to bfloat16, both to nearest even.
+// A head row holding a NaN or an infinity is a lost row: scale = the float32
+// quiet NaN 0x7FC00000 and every code 0 (its largest 15-bit magnitude is
+// 0x7F80 or more, so the amax reduction finds it for free); a row whose scale
+// is not finite is dequantised to the bfloat16 quiet NaN 0x7FC0 throughout.
 // Every step is a single IEEE operation with an explicit rounding mode
 // (__fdiv_rn, __fmul_rn, __float2int_rn, the cvt.rn.satfinite conversions),
 // so the integer decisions are the same on any correctly rounding machine.
@@ -27,8 +31,11 @@
 // elements.  amax is reduced within the group with xor shuffles on the
 // 15-bit magnitudes of the bfloat16 patterns (for non-NaN values the order of
 // |x| is the integer order of those bits).  Each group keeps kQuantRows head
-// rows' loads in flight.  Blocks are kQuantThreads threads, whole warps, so
-// every shuffle runs with all 32 lanes present.
+// rows' loads in flight when quantising (kQuantRowsShort on the 8-element
+// path when a lane holds at most 2 vectors of a row; kDequantRows when
+// dequantising).
+// Blocks are kQuantThreads (kDequantThreads) threads, whole warps, so every
+// shuffle runs with all 32 lanes present.
 //
 // The kernels are bound by instruction issue before HBM unless every
 // per-element step is a single cheap instruction, so the 8-element path
@@ -47,7 +54,20 @@
 //   * the row index (token, head) of a group: n / heads by a multiply-high
 //     and a shift (the round-up method of Granlund and Montgomery, "Division
 //     by invariant integers using multiplication", 1994), exact for
-//     n < 2^31.
+//     n < 2^31;
+//   * inv = top / amax and scale = amax / top without a division per row:
+//     a live amax is a normal bfloat16, M * 2^k with M = 1 + j/128 (j = its 7
+//     stored mantissa bits), and scaling by a power of two commutes with
+//     float32 rounding while the result stays normal, so
+//     fl(top / amax) = fl(top / M) * 2^-k and fl(amax / top) = fl(M / top) * 2^k
+//     exactly.  Each block computes the 128 values fl(top / M) and fl(M / top)
+//     with the correctly rounded division into shared memory once; a row then
+//     takes two table reads and two additions to the exponent field.  For
+//     amax in [2^-96, 2^128) both results stay normal (inv within
+//     [2^-121, 2^105], scale within [2^-105, 2^121]).  Unlike a division per
+//     row, the cost does not depend on the data (a correctly rounded division
+//     by an amax of 2^126 or more, whose reciprocal is subnormal, is several
+//     times slower).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -61,9 +81,40 @@ namespace vf {
 #ifndef VF_QUANT_ROWS
 #define VF_QUANT_ROWS 2
 #endif
+#ifndef VF_QUANT_ROWS_SHORT
+#define VF_QUANT_ROWS_SHORT 3
+#endif
+#ifndef VF_DEQUANT_ROWS
+#define VF_DEQUANT_ROWS 1
+#endif
+#ifndef VF_QUANT_THREADS
+#define VF_QUANT_THREADS 128
+#endif
+#ifndef VF_DEQUANT_THREADS
+#define VF_DEQUANT_THREADS 256
+#endif
 
-constexpr int kQuantThreads = 256;         // threads per block (8 full warps)
-constexpr int kQuantRows = VF_QUANT_ROWS;  // head rows per group in flight
+constexpr int kQuantThreads = VF_QUANT_THREADS;      // threads per block, quantising
+constexpr int kDequantThreads = VF_DEQUANT_THREADS;  // threads per block, dequantising
+constexpr int kQuantRows = VF_QUANT_ROWS;        // head rows per group in flight, quantising
+constexpr int kQuantRowsShort = VF_QUANT_ROWS_SHORT;   // the same, 8-element path, <= 2 vectors
+                                                       // per lane (short head rows)
+constexpr int kDequantRows = VF_DEQUANT_ROWS;    // the same, dequantising
+static_assert(kQuantThreads % 32 == 0 && kDequantThreads % 32 == 0,
+              "blocks are whole warps");
+#ifndef VF_QUANT_F32X2
+#define VF_QUANT_F32X2 1
+#endif
+#ifndef VF_QUANT_DIV_TABLE
+#define VF_QUANT_DIV_TABLE 1
+#endif
+constexpr int kMantissas = 128;            // bfloat16 stored-mantissa patterns
+
+// Head rows in flight per group on the 8-element quantising path with NV
+// vectors per lane.
+__host__ __device__ constexpr int quant_rows8(int NV) {
+    return NV >= 4 ? kQuantRows : kQuantRowsShort;
+}
 constexpr int kMaxQPieces = 128;           // pieces per launch (parameter space)
 
 constexpr int kFmtInt8 = 1;
@@ -98,6 +149,17 @@ template <> struct QVec<1> { using B = unsigned short; using C = unsigned char; 
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) {
     return __uint_as_float(h << 16);
+}
+
+constexpr uint32_t kLostScaleBits = 0x7FC00000u;   // scale of a lost row (float32 quiet NaN)
+constexpr uint32_t kLostValue2 = 0x7FC07FC0u;      // two bfloat16 quiet NaNs
+
+// A 15-bit bfloat16 magnitude of a NaN or an infinity.
+__device__ __forceinline__ bool non_finite_magnitude(uint32_t m) { return m >= 0x7F80u; }
+
+// A scale that is NaN or an infinity: its row is written as NaN.
+__device__ __forceinline__ bool lost_scale(float s) {
+    return (__float_as_uint(s) & 0x7FFFFFFFu) >= 0x7F800000u;
 }
 
 template <int FMT>
@@ -172,10 +234,32 @@ __device__ __forceinline__ uint32_t rint_bits(float q) {
     return __float_as_uint(__fadd_rn(q, 12582912.0f));
 }
 
+// Two float32 products, each rounded once to nearest even: the packed f32x2
+// form of sm_100 and later issues both in one instruction.  Used only where a
+// conversion, never an addition, consumes the products: measured on GB300,
+// ptxas fuses a packed multiply and a packed add that follows it into one
+// fused multiply-add even when both carry an explicit .rn, which rounds once
+// where the format rounds twice (q = x * inv exactly 63.5 after its own
+// rounding came out 63).  The INT8 encoder therefore keeps the scalar
+// __fmul_rn / __fadd_rn, which are never contracted.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+#if VF_QUANT_F32X2
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+#else
+    return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
+#endif
+}
+
 // Eight bfloat16 patterns -> eight codes.
 template <int FMT>
 __device__ __forceinline__ uint2 encode8(const uint4 &w, float inv) {
     const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    const float2 inv2 = make_float2(inv, inv);
     uint32_t out[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -183,8 +267,16 @@ __device__ __forceinline__ uint2 encode8(const uint4 &w, float inv) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const uint32_t x = in[2 * k + j];
-            f[2 * j] = __fmul_rn(__uint_as_float(x << 16), inv);          // element 2j
-            f[2 * j + 1] = __fmul_rn(__uint_as_float(x & 0xFFFF0000u), inv);
+            // elements 2j (low half) and 2j + 1 (high half) of the pair
+            const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xFFFF0000u);
+            if constexpr (FMT == kFmtInt8) {
+                f[2 * j] = __fmul_rn(lo, inv);
+                f[2 * j + 1] = __fmul_rn(hi, inv);
+            } else {
+                const float2 q = mul2_rn(make_float2(lo, hi), inv2);
+                f[2 * j] = q.x;
+                f[2 * j + 1] = q.y;
+            }
         }
         if constexpr (FMT == kFmtInt8) {
             const uint32_t b01 = __byte_perm(rint_bits(f[0]), rint_bits(f[1]), 0x0040);
@@ -220,8 +312,11 @@ __device__ __forceinline__ uint2 decode4(uint32_t c, float s) {
         const float2 b = __half22float2(__half2(hi));
         f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
     }
-    const __nv_bfloat162 y01 = __floats2bfloat162_rn(__fmul_rn(f[0], s), __fmul_rn(f[1], s));
-    const __nv_bfloat162 y23 = __floats2bfloat162_rn(__fmul_rn(f[2], s), __fmul_rn(f[3], s));
+    const float2 s2 = make_float2(s, s);
+    const float2 p01 = mul2_rn(make_float2(f[0], f[1]), s2);
+    const float2 p23 = mul2_rn(make_float2(f[2], f[3]), s2);
+    const __nv_bfloat162 y01 = __floats2bfloat162_rn(p01.x, p01.y);
+    const __nv_bfloat162 y23 = __floats2bfloat162_rn(p23.x, p23.y);
     return make_uint2(*reinterpret_cast<const uint32_t *>(&y01),
                       *reinterpret_cast<const uint32_t *>(&y23));
 }
@@ -286,11 +381,14 @@ quantise_rows(const __grid_constant__ QArgs a) {
             const uint32_t hr = base + group + uint32_t(r) * groups;
             if (hr >= nrows) continue;
             const float amax = bf16_bits_to_float(m[r]);
-            const bool live = amax >= 0x1p-96f;
+            const bool lost = non_finite_magnitude(m[r]);
+            const bool live = !lost && amax >= 0x1p-96f;
             const float inv = live ? __fdiv_rn(top, amax) : 0.0f;
             const int64_t prow = pc.first_row + hr;               // packed head row
             uint8_t *crow = a.codes + prow * a.D;
-            if (lane == 0) a.scales[prow] = live ? __fdiv_rn(amax, top) : 0.0f;
+            if (lane == 0)
+                a.scales[prow] = lost ? __uint_as_float(kLostScaleBits)
+                                      : live ? __fdiv_rn(amax, top) : 0.0f;
             if (kOne) {
                 if (int(lane) >= a.nvec) continue;
                 uint8_t c[VW];
@@ -317,7 +415,7 @@ quantise_rows(const __grid_constant__ QArgs a) {
 
 // Merge or unpack with dequantisation.  Same grid and groups; no reduction.
 template <int VW, int FMT>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kDequantThreads)
 dequantise_rows(const __grid_constant__ QArgs a) {
     using B = typename QVec<VW>::B;
     using CV = typename QVec<VW>::C;
@@ -325,18 +423,18 @@ dequantise_rows(const __grid_constant__ QArgs a) {
     const QPiece &pc = a.pieces[blockIdx.y];
     const uint32_t G = 1u << a.lanes_log2;
     const uint32_t lane = threadIdx.x & (G - 1);
-    const uint32_t groups = kQuantThreads >> a.lanes_log2;
+    const uint32_t groups = kDequantThreads >> a.lanes_log2;
     const uint32_t group = threadIdx.x >> a.lanes_log2;
     const uint32_t nrows = uint32_t(pc.rows) * uint32_t(a.heads);
 
-    for (uint32_t base = blockIdx.x * groups * kQuantRows; base < nrows;
-         base += gridDim.x * groups * kQuantRows) {
-        CV cv[kQuantRows];
-        float sc[kQuantRows];
+    for (uint32_t base = blockIdx.x * groups * kDequantRows; base < nrows;
+         base += gridDim.x * groups * kDequantRows) {
+        CV cv[kDequantRows];
+        float sc[kDequantRows];
         // one vector per lane per row on the fast path; loads first
         if (int(G) * 1 >= a.nvec) {
 #pragma unroll
-            for (int r = 0; r < kQuantRows; ++r) {
+            for (int r = 0; r < kDequantRows; ++r) {
                 const uint32_t hr = base + group + uint32_t(r) * groups;
                 if (hr < nrows && int(lane) < a.nvec) {
                     const int64_t prow = pc.first_row + hr;
@@ -346,27 +444,30 @@ dequantise_rows(const __grid_constant__ QArgs a) {
                 }
             }
 #pragma unroll
-            for (int r = 0; r < kQuantRows; ++r) {
+            for (int r = 0; r < kDequantRows; ++r) {
                 const uint32_t hr = base + group + uint32_t(r) * groups;
                 if (hr >= nrows || int(lane) >= a.nvec) continue;
                 uint8_t c[VW];
                 memcpy(c, &cv[r], sizeof(c));
+                const bool lost = lost_scale(sc[r]);
                 uint16_t y[VW];
 #pragma unroll
                 for (int i = 0; i < VW; ++i)
-                    y[i] = __bfloat16_as_ushort(
-                        __float2bfloat16_rn(__fmul_rn(code_value<FMT>(c[i]), sc[r])));
+                    y[i] = lost ? uint16_t(kLostValue2 & 0xFFFFu)
+                                : __bfloat16_as_ushort(__float2bfloat16_rn(
+                                      __fmul_rn(code_value<FMT>(c[i]), sc[r])));
                 B out;
                 memcpy(&out, y, sizeof(out));
                 *reinterpret_cast<B *>(pc.strided + strided_offset(a, hr, int64_t(lane) * VW)) =
                     out;
             }
         } else {
-            for (int r = 0; r < kQuantRows; ++r) {
+            for (int r = 0; r < kDequantRows; ++r) {
                 const uint32_t hr = base + group + uint32_t(r) * groups;
                 if (hr >= nrows) continue;
                 const int64_t prow = pc.first_row + hr;
                 const float s = a.scales[prow];
+                const bool lost = lost_scale(s);
                 uint16_t *row = pc.strided + strided_offset(a, hr, 0);
                 for (int v = int(lane); v < a.nvec; v += int(G)) {
                     const CV x = *reinterpret_cast<const CV *>(a.codes + prow * a.D +
@@ -376,8 +477,9 @@ dequantise_rows(const __grid_constant__ QArgs a) {
                     uint16_t y[VW];
 #pragma unroll
                     for (int i = 0; i < VW; ++i)
-                        y[i] = __bfloat16_as_ushort(
-                            __float2bfloat16_rn(__fmul_rn(code_value<FMT>(c[i]), s)));
+                        y[i] = lost ? uint16_t(kLostValue2 & 0xFFFFu)
+                                    : __bfloat16_as_ushort(__float2bfloat16_rn(
+                                          __fmul_rn(code_value<FMT>(c[i]), s)));
                     B out;
                     memcpy(&out, y, sizeof(out));
                     *reinterpret_cast<B *>(row + int64_t(v) * VW * a.d_stride) = out;
@@ -393,6 +495,19 @@ dequantise_rows(const __grid_constant__ QArgs a) {
 template <int FMT, int NV>
 __global__ void __launch_bounds__(kQuantThreads)
 quantise_rows8(const __grid_constant__ QArgs a) {
+    constexpr int kRows = quant_rows8(NV);
+    const float top = top_code<FMT>();
+#if VF_QUANT_DIV_TABLE
+    // fl(top / M) and fl(M / top) for the 128 mantissas M = 1 + j/128, built
+    // before the grid-dependency wait (it overlaps the previous grid's tail)
+    __shared__ float inv_of[kMantissas], scale_of[kMantissas];
+    for (int j = int(threadIdx.x); j < kMantissas; j += kQuantThreads) {
+        const float M = 1.0f + float(j) * (1.0f / 128.0f);      // exact
+        inv_of[j] = __fdiv_rn(top, M);
+        scale_of[j] = __fdiv_rn(M, top);
+    }
+    __syncthreads();
+#endif
     wait_for_previous_grid();
     const QPiece &pc = a.pieces[blockIdx.y];
     const uint32_t G = 1u << a.lanes_log2;
@@ -401,14 +516,13 @@ quantise_rows8(const __grid_constant__ QArgs a) {
     const uint32_t group = threadIdx.x >> a.lanes_log2;
     const uint32_t nrows = uint32_t(pc.rows) * uint32_t(a.heads);   // < 2^31, host-checked
     const uint32_t nvec = uint32_t(a.nvec);
-    const float top = top_code<FMT>();
 
-    for (uint32_t base = blockIdx.x * groups * kQuantRows; base < nrows;
-         base += gridDim.x * groups * kQuantRows) {
-        uint4 w[kQuantRows][NV];
-        uint32_t m[kQuantRows];
+    for (uint32_t base = blockIdx.x * groups * kRows; base < nrows;
+         base += gridDim.x * groups * kRows) {
+        uint4 w[kRows][NV];
+        uint32_t m[kRows];
 #pragma unroll
-        for (int r = 0; r < kQuantRows; ++r) {
+        for (int r = 0; r < kRows; ++r) {
             const uint32_t hr = base + group + uint32_t(r) * groups;
             const uint16_t *row = pc.strided + strided_offset(a, hr, 0);
             m[r] = 0;
@@ -424,21 +538,34 @@ quantise_rows8(const __grid_constant__ QArgs a) {
         }
         // group-wide amax: all 32 lanes of every warp are here
 #pragma unroll
-        for (int r = 0; r < kQuantRows; ++r) {
+        for (int r = 0; r < kRows; ++r) {
             for (uint32_t o = G >> 1; o > 0; o >>= 1)
                 m[r] = max_u16x2(m[r], __shfl_xor_sync(0xFFFFFFFFu, m[r], int(o)));
             m[r] = max(m[r] & 0xFFFFu, m[r] >> 16);
         }
 #pragma unroll
-        for (int r = 0; r < kQuantRows; ++r) {
+        for (int r = 0; r < kRows; ++r) {
             const uint32_t hr = base + group + uint32_t(r) * groups;
             if (hr >= nrows) continue;
+            // m[r]: the row's largest magnitude as a bfloat16 pattern
+            const bool lost = non_finite_magnitude(m[r]);
+            const bool live = !lost && m[r] >= 0x0F80u;           // amax >= 2^-96 (31 << 7)
+#if VF_QUANT_DIV_TABLE
+            // amax = M * 2^k: mantissa index j, exponent k = e - 127
+            const uint32_t j = m[r] & 0x7Fu;
+            const uint32_t k23 = uint32_t((int32_t(m[r] >> 7) - 127) * (1 << 23));  // k << 23
+            const float inv = live ? __uint_as_float(__float_as_uint(inv_of[j]) - k23) : 0.0f;
+            const float scale = __uint_as_float(__float_as_uint(scale_of[j]) + k23);
+#else
             const float amax = bf16_bits_to_float(m[r]);
-            const bool live = amax >= 0x1p-96f;
             const float inv = live ? __fdiv_rn(top, amax) : 0.0f;
+            const float scale = live ? __fdiv_rn(amax, top) : 0.0f;
+#endif
             const int64_t prow = pc.first_row + hr;               // packed head row
             uint8_t *crow = a.codes + prow * a.D;
-            if (lane == 0) a.scales[prow] = live ? __fdiv_rn(amax, top) : 0.0f;
+            if (lane == 0)
+                a.scales[prow] = lost ? __uint_as_float(kLostScaleBits)
+                                      : live ? scale : 0.0f;
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
                 const uint32_t v = lane + uint32_t(j) * G;
@@ -452,23 +579,23 @@ quantise_rows8(const __grid_constant__ QArgs a) {
 }
 
 template <int FMT, int NV>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kDequantThreads)
 dequantise_rows8(const __grid_constant__ QArgs a) {
     wait_for_previous_grid();
     const QPiece &pc = a.pieces[blockIdx.y];
     const uint32_t G = 1u << a.lanes_log2;
     const uint32_t lane = threadIdx.x & (G - 1);
-    const uint32_t groups = kQuantThreads >> a.lanes_log2;
+    const uint32_t groups = kDequantThreads >> a.lanes_log2;
     const uint32_t group = threadIdx.x >> a.lanes_log2;
     const uint32_t nrows = uint32_t(pc.rows) * uint32_t(a.heads);
     const uint32_t nvec = uint32_t(a.nvec);
 
-    for (uint32_t base = blockIdx.x * groups * kQuantRows; base < nrows;
-         base += gridDim.x * groups * kQuantRows) {
-        uint2 c[kQuantRows][NV];
-        float sc[kQuantRows];
+    for (uint32_t base = blockIdx.x * groups * kDequantRows; base < nrows;
+         base += gridDim.x * groups * kDequantRows) {
+        uint2 c[kDequantRows][NV];
+        float sc[kDequantRows];
 #pragma unroll
-        for (int r = 0; r < kQuantRows; ++r) {
+        for (int r = 0; r < kDequantRows; ++r) {
             const uint32_t hr = base + group + uint32_t(r) * groups;
             const int64_t prow = pc.first_row + hr;
             sc[r] = hr < nrows ? a.scales[prow] : 0.0f;
@@ -482,10 +609,20 @@ dequantise_rows8(const __grid_constant__ QArgs a) {
             }
         }
 #pragma unroll
-        for (int r = 0; r < kQuantRows; ++r) {
+        for (int r = 0; r < kDequantRows; ++r) {
             const uint32_t hr = base + group + uint32_t(r) * groups;
             if (hr >= nrows) continue;
             uint16_t *row = pc.strided + strided_offset(a, hr, 0);
+            if (lost_scale(sc[r])) {                          // rare: a lost row
+#pragma unroll
+                for (int j = 0; j < NV; ++j) {
+                    const uint32_t v = lane + uint32_t(j) * G;
+                    if (v < nvec)
+                        *reinterpret_cast<uint4 *>(row + int64_t(v) * 8) =
+                            make_uint4(kLostValue2, kLostValue2, kLostValue2, kLostValue2);
+                }
+                continue;
+            }
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
                 const uint32_t v = lane + uint32_t(j) * G;

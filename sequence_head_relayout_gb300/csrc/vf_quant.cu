@@ -20,19 +20,28 @@ static_assert(vf::kFmtInt8 == VF_FORMAT_INT8 && vf::kFmtE4M3 == VF_FORMAT_E4M3,
 
 constexpr int64_t kMaxGridX = int64_t(1) << 20;   // the kernels stride over head rows
 
-// 16-byte vectors per lane on the 8-element path, quantising and
-// dequantising (tuning constants).  Measured on GB300 over 1, 2 and 4 vectors
-// and 1, 2 and 4 head rows in flight per group: quantising is fastest at 4
-// vectors and 2 rows (the per-row reduction and divisions amortised over 32
-// elements per lane), dequantising at 2 vectors and 1-2 rows.
-#ifndef VF_QUANT_NV
-#define VF_QUANT_NV 4
+// 16-byte vectors per lane on the 8-element path (tuning constants).
+// Quantising, a head row is shared by a group of about kQuantLanes lanes,
+// each holding 1, 2 or 4 vectors of it (the fewest that let kQuantLanes lanes
+// cover the row); dequantising, every lane holds kDequantNV vectors.
+// Measured on GB300 (pages', ragged and large workloads): groups of 4 lanes
+// beat 2 and 8 at both D = 64 and D = 128.
+#ifndef VF_QUANT_LANES
+#define VF_QUANT_LANES 4
 #endif
 #ifndef VF_DEQUANT_NV
 #define VF_DEQUANT_NV 2
 #endif
-constexpr int kQuantNV = VF_QUANT_NV;
+constexpr int64_t kQuantLanes = VF_QUANT_LANES;
+constexpr int kQuantMaxNV = 4;
 constexpr int kDequantNV = VF_DEQUANT_NV;
+
+// Vectors per lane when quantising a head row of nvec 16-byte vectors.
+int quant_nv(int64_t nvec) {
+    if (nvec <= kQuantLanes) return 1;
+    if (nvec <= 2 * kQuantLanes) return 2;
+    return kQuantMaxNV;
+}
 
 // Multiplier and shift with n / d == (umulhi(n, mul) + n) >> shift for all
 // n < 2^31 and 1 <= d < 2^31 (Granlund and Montgomery's round-up method):
@@ -66,8 +75,8 @@ int pick_vector_width(const Plan &pl) {
 }
 
 // kPath: 0 = generic, one vector per lane; 1 = generic, per-lane loop;
-// 2 = the 8-element path with kQuantNV or kDequantNV vectors per lane.
-template <int VW, int FMT, int kPath>
+// 2 = the 8-element path with NV vectors per lane.
+template <int VW, int FMT, int kPath, int NV = 1>
 int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
     vf::QArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -81,7 +90,10 @@ int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
     a.lanes_log2 = lanes_log2;
     a.nvec = int32_t(pl.D / VW);
     fast_divisor(std::max<int64_t>(pl.heads, 1), &a.div_mul, &a.div_shift);
-    const int64_t rows_per_block = int64_t(vf::kQuantThreads >> lanes_log2) * vf::kQuantRows;
+    const int threads = pl.quantise ? vf::kQuantThreads : vf::kDequantThreads;
+    const int rows = !pl.quantise ? vf::kDequantRows
+                     : kPath == 2 ? vf::quant_rows8(NV) : vf::kQuantRows;
+    const int64_t rows_per_block = int64_t(threads >> lanes_log2) * rows;
 
     const size_t n = pl.pieces.size();
     for (size_t first = 0; first < n; first += vf::kMaxQPieces) {
@@ -95,7 +107,7 @@ int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
         cudaLaunchConfig_t cfg = {};
         const int64_t gx = std::min(kMaxGridX, (max_hr + rows_per_block - 1) / rows_per_block);
         cfg.gridDim = dim3(unsigned(gx), unsigned(cnt), 1);
-        cfg.blockDim = dim3(unsigned(vf::kQuantThreads), 1, 1);
+        cfg.blockDim = dim3(unsigned(threads), 1, 1);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -106,7 +118,7 @@ int launch_family(const Plan &pl, int lanes_log2, cudaStream_t stream) {
         cudaError_t e;
         if constexpr (kPath == 2) {
             if (pl.quantise)
-                e = cudaLaunchKernelEx(&cfg, vf::quantise_rows8<FMT, kQuantNV>, a);
+                e = cudaLaunchKernelEx(&cfg, vf::quantise_rows8<FMT, NV>, a);
             else
                 e = cudaLaunchKernelEx(&cfg, vf::dequantise_rows8<FMT, kDequantNV>, a);
         } else {
@@ -134,9 +146,18 @@ int lanes_log2_for(int64_t nvec, int64_t per_lane) {
 template <int VW, int FMT>
 int launch_vw(const Plan &pl, cudaStream_t stream) {
     const int64_t nvec = pl.D / VW;
-    const int64_t nv = pl.quantise ? kQuantNV : kDequantNV;
-    if (VW == 8 && nvec <= 32 * nv)
-        return launch_family<VW, FMT, 2>(pl, lanes_log2_for(nvec, nv), stream);
+    if (VW == 8 && pl.quantise && nvec <= 32 * kQuantMaxNV) {
+        switch (quant_nv(nvec)) {
+            case 1: return launch_family<VW, FMT, 2, 1>(pl, lanes_log2_for(nvec, 1), stream);
+            case 2: return launch_family<VW, FMT, 2, 2>(pl, lanes_log2_for(nvec, 2), stream);
+            default:
+                return launch_family<VW, FMT, 2, kQuantMaxNV>(
+                    pl, lanes_log2_for(nvec, kQuantMaxNV), stream);
+        }
+    }
+    if (VW == 8 && !pl.quantise && nvec <= 32 * kDequantNV)
+        return launch_family<VW, FMT, 2, kDequantNV>(pl, lanes_log2_for(nvec, kDequantNV),
+                                                     stream);
     const int lg = lanes_log2_for(nvec, 1);
     const bool one = nvec <= (int64_t(1) << lg);
     if (one || !pl.quantise) return launch_family<VW, FMT, 0>(pl, lg, stream);

@@ -209,3 +209,35 @@ def finite_rows_(view: torch.Tensor, seed: int) -> torch.Tensor:
             x[r, ::3] = 2.0 ** -130                       # bf16 denormal
     view.copy_(x.to(torch.bfloat16).view(torch.int16).view(view.shape))
     return view
+
+
+# Non-finite 16-bit patterns planted by plant_non_finite_: a quiet NaN, +inf,
+# -inf, a negative NaN with payload, a signalling-NaN payload.
+NON_FINITE_BITS = (0x7FC0, 0x7F80, 0xFF80, 0xFFC1, 0x7F81)
+
+
+def plant_non_finite_(view: torch.Tensor, seed: int, every: int = 97) -> torch.Tensor:
+    """Overwrite one element in every `every`-th D-element row of a 16-bit view
+    [..., D] (rows in logical order, starting at a seeded row) with a
+    non-finite pattern (NON_FINITE_BITS in turn), at a seeded position in the
+    row.  Returns the view."""
+    D = view.shape[-1]
+    rows = view.numel() // D if D else 0
+    if rows == 0:
+        return view
+    g = torch.Generator()
+    g.manual_seed(seed)
+    first = int(torch.randint(0, min(every, rows), (1,), generator=g))
+    idx = torch.arange(first, rows, every)
+    pos = torch.randint(0, D, (idx.numel(),), generator=g)
+    vals = torch.tensor([_as_i16(NON_FINITE_BITS[i % len(NON_FINITE_BITS)])
+                         for i in range(idx.numel())], dtype=torch.int16)
+    flat = view.reshape(rows, D) if view.is_contiguous() else None
+    if flat is not None:
+        flat[idx.to(view.device), pos.to(view.device)] = vals.to(view.device)
+    else:
+        lead = view.shape[:-1]
+        coords = torch.unravel_index(idx, lead)
+        view[tuple(c.to(view.device) for c in coords) + (pos.to(view.device),)] = \
+            vals.to(view.device)
+    return view
