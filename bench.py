@@ -41,6 +41,7 @@ METRIC = "effective HBM GB/s (read+write) and % of GB300 peak per relayout op"
 UNIT = "GB/s"
 WORKLOAD = "pages"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900
 # what the GPU executes: the kernel and its launch policy (not the ABI's checks)
 KERNEL_SOURCES = ["sequence_head_relayout_gb300/csrc/relayout_kernel.cuh",
                   "sequence_head_relayout_gb300/csrc/launch.cuh"]
@@ -138,6 +139,24 @@ def _oracle_proc(rank, shape, passes, barrier, results):
     results.put((rank, times))
 
 
+def _collect(results, n: int, procs, timeout_s: float = 900.0):
+    """n results from spawned workers; raises if a worker died or the
+    results do not arrive within timeout_s."""
+    import queue
+    got, t0 = [], time.monotonic()
+    while len(got) < n:
+        try:
+            got.append(results.get(timeout=2.0))
+        except queue.Empty:
+            dead = [pr.exitcode for pr in procs if pr.exitcode not in (None, 0)]
+            if dead or time.monotonic() - t0 > timeout_s:
+                for pr in procs:
+                    if pr.is_alive():
+                        pr.terminate()
+                raise RuntimeError("CPU oracle workers failed (exit codes %s)" % dead)
+    return got
+
+
 def run_oracle(cfg, tokens: int, passes: int, cores: int):
     """Per-pass times (the slowest core's) of `cores` processes, each moving
     its own `tokens`-token sample; and the bytes all cores move per pass."""
@@ -151,7 +170,7 @@ def run_oracle(cfg, tokens: int, passes: int, cores: int):
              for r in range(cores)]
     for pr in procs:
         pr.start()
-    got = [results.get() for _ in procs]
+    got = _collect(results, cores, procs)
     for pr in procs:
         pr.join()
     per_pass = [max(t[i] for _, t in got) for i in range(passes)]
@@ -240,16 +259,161 @@ def cpu_baseline(cfg, budget_s: float = 10.0, cores: int = None):
     passes = int(max(3, min(30, budget_s / max(est, 1e-3))))
     per_pass, nbytes = run_oracle(cfg, tokens, passes, cores)
     total = sum(per_pass)
-    one, one_bytes = run_oracle(cfg, tokens, 2, 1)
-    return {"value": round(passes * nbytes / total / 1e9, 3), "unit": UNIT, "cores": cores,
-            "kind": "oracle",
-            "single_core_value": round(2 * one_bytes / sum(one) / 1e9, 3),
+    one, one_bytes = run_oracle(cfg, tokens, 3, 1)
+    return {"value": round(nbytes / statistics.median(per_pass) / 1e9, 3), "unit": UNIT,
+            "cores": cores, "kind": "oracle",
+            "single_core_value": round(one_bytes / statistics.median(one) / 1e9, 3),
             "cpu_model": cpu_model(),
+            "statistic": "median pass",
             "sample": "%d of %d tokens (H=%d, D=%d, P=%d, C=%d, padded-row pack source, "
                       "head-major split source) per core, one process per core, %d timed "
                       "passes of pack+split+merge started together, %.1f s; single core: "
-                      "2 passes of the same sample"
+                      "3 passes of the same sample"
                       % (tokens, cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, passes, total)}
+
+
+CPU_OPS = ("qkv_pack", "attn_split", "head_merge", "qkv_unpack")
+CPU_SAMPLE_BYTES = 256 << 20     # inputs + outputs of the four ops held by one process
+CPU_MIN_PASS_ELEMS = 1 << 22     # elements one timed pass moves at least (repeating the op)
+
+
+def cpu_sample_tokens(cfg, cap_bytes: int = CPU_SAMPLE_BYTES) -> int:
+    """Tokens of a per-process sample of `cfg`: the whole workload when its
+    four ops' inputs and outputs fit in cap_bytes, else the first tokens that
+    do."""
+    H, D, Hp = cfg.H, cfg.D, cfg.H // cfg.P
+    per_token = 2 * ((3 * H * D + cfg.pad) + 3 * H * D + 4 * H * D + 6 * Hp * D)
+    return int(max(1, min(cfg.T, cap_bytes // per_token)))
+
+
+def _cpu_op_inputs(shape, T, seed):
+    """numpy buffers and element strides of the four ops on a T-token sample,
+    in the workload's own layouts (padded or head-major pack source,
+    head-major split source, head-major merge destination)."""
+    import numpy as np
+    H, D, P, C, pad, pack_src, split_src, merge_dst = shape
+    Hp = H // P
+    rng = np.random.default_rng(seed)
+
+    def bits(n):
+        return rng.integers(0, 1 << 16, size=n, dtype=np.uint16)
+
+    row = 3 * H * D + pad
+    x = {"pack_src": bits(T * row), "pack_dst": np.empty(3 * T * H * D, np.uint16),
+         "split_src": bits(T * H * D), "split_dst": np.empty(T * H * D, np.uint16),
+         "merge_src": bits(T * H * D), "merge_dst": np.empty(T * H * D, np.uint16),
+         "recv": bits(3 * T * Hp * D)}
+    for k in ("q", "k", "v"):
+        x[k] = np.empty(T * Hp * D, np.uint16)
+    st = {"pack": (row, H * D, D, 1) if pack_src != "head_major" else (row, D, 3 * D, 1),
+          "split": (D, T * D, 1) if split_src == "bhtd" else (H * D, D, 1),
+          "merge": (D, T * D, 1) if merge_dst == "head_major" else (H * D, D, 1),
+          "unpack": (Hp * D, D, 1)}
+    return x, st
+
+
+def _cpu_op_worker(rank, tasks, barrier, results):
+    """One host process: for every task (a workload sample), build its inputs
+    once, then time each op `passes` times, every pass started together with
+    the other processes (barrier)."""
+    import ctypes
+
+    from oracle import build
+    lib = ctypes.CDLL(build.LIB)
+    I64 = ctypes.c_int64
+    for f in (lib.oracle_qkv_pack, lib.oracle_attn_split, lib.oracle_head_merge,
+              lib.oracle_qkv_unpack_recv):
+        f.restype = I64
+    while True:
+        task = tasks.get()
+        if task is None:
+            return
+        key, shape, T, passes, reps = task
+        H, D, P, C = shape[:4]
+        x, st = _cpu_op_inputs(shape, T, 5000 + rank)
+        ptr = {k: ctypes.c_void_p(v.ctypes.data) for k, v in x.items()}
+        arr = {k: (I64 * len(v))(*v) for k, v in st.items()}
+        dims = (I64(T), I64(H), I64(D), I64(P), I64(C))
+        run = {
+            "qkv_pack": lambda: lib.oracle_qkv_pack(ptr["pack_src"], arr["pack"], *dims,
+                                                    ptr["pack_dst"]),
+            "attn_split": lambda: lib.oracle_attn_split(ptr["split_src"], arr["split"], *dims,
+                                                        ptr["split_dst"]),
+            "head_merge": lambda: lib.oracle_head_merge(ptr["merge_src"], *dims,
+                                                        ptr["merge_dst"], arr["merge"]),
+            "qkv_unpack": lambda: lib.oracle_qkv_unpack_recv(ptr["recv"], *dims, ptr["q"],
+                                                             ptr["k"], ptr["v"], arr["unpack"]),
+        }
+        times = {}
+        for op in CPU_OPS:
+            times[op] = []
+            for _ in range(passes):
+                barrier.wait()
+                t0 = time.perf_counter()
+                for _ in range(reps[op]):
+                    n = run[op]()
+                times[op].append(time.perf_counter() - t0)
+                if n < 0:
+                    raise RuntimeError("oracle %s rejected the sample" % op)
+        del x, ptr
+        results.put((rank, key, times))
+
+
+def cpu_per_config(names, cores: int = None, passes: int = 3):
+    """The C oracle, unmodified, timed per op at every workload: on all host
+    cores (one spawned process per core, each moving its own sample, every
+    pass started together; a pass takes the slowest process's time) and on one
+    core; median of `passes`.  GB/s counts the same algorithmic bytes as the
+    GPU figures (4 B per element moved), summed over processes."""
+    from oracle import build
+    from sequence_head_relayout_gb300 import workloads as W
+    build.build()
+    cores = cores or os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    table = {name: {} for name in names}
+    samples = {}
+    t_all = time.perf_counter()
+    for nproc in (cores, 1):
+        barrier = ctx.Barrier(nproc)
+        tasks, results = ctx.Queue(), ctx.Queue()
+        procs = [ctx.Process(target=_cpu_op_worker, args=(r, tasks, barrier, results))
+                 for r in range(nproc)]
+        for pr in procs:
+            pr.start()
+        for name in names:
+            cfg = W.CONFIGS[name]
+            T = cpu_sample_tokens(cfg)
+            samples[name] = T
+            shape = (cfg.H, cfg.D, cfg.P, cfg.C, cfg.pad, cfg.pack_src, cfg.split_src,
+                     cfg.merge_dst)
+            sample_cfg = W.Config(name, T, cfg.H, cfg.D, cfg.P, cfg.C)
+            elems = op_elements(sample_cfg)
+            # small samples repeat the op inside a pass (about 4 M elements moved)
+            reps = {op: max(1, CPU_MIN_PASS_ELEMS // max(1, elems[op])) for op in CPU_OPS}
+            for _ in range(nproc):
+                tasks.put((name, shape, T, passes, reps))
+            got = _collect(results, nproc, procs)
+            for op in CPU_OPS:
+                per_pass = [max(t[op][i] for _, _, t in got) for i in range(passes)]
+                med = statistics.median(per_pass)
+                gbs = nproc * reps[op] * alg_bytes(elems[op]) / med / 1e9
+                key = "cpu_gbs" if nproc == cores else "cpu_gbs_1core"
+                table[name].setdefault(op, {})[key] = round(gbs, 3)
+        for _ in range(nproc):
+            tasks.put(None)
+        for pr in procs:
+            pr.join()
+    desc = {name: "%d of %d tokens per process%s" % (samples[name], W.CONFIGS[name].T,
+                                                    "" if samples[name] == W.CONFIGS[name].T
+                                                    else " (sampled)")
+            for name in names}
+    return {"cores": cores, "cpu_model": cpu_model(), "kind": "oracle",
+            "statistic": "median of %d passes; an all-core pass is timed from a common "
+                         "start to the slowest process's end" % passes,
+            "parallelism": "one spawned process per core, each moving its own sample "
+                           "(the oracle has no threading of its own)",
+            "sample": desc, "seconds": round(time.perf_counter() - t_all, 1),
+            "table": table}
 
 
 # ----------------------------------------------------------------------------
@@ -372,6 +536,41 @@ def make_set(cfg, dev, seed_shift, ops=("qkv_pack", "attn_split", "head_merge"))
     return s
 
 
+def run_op(vf, cfg, s, name):
+    """Enqueue one relayout of the step on the current stream."""
+    if name == "qkv_pack":
+        vf.qkv_pack(s["pack_src"], cfg.P, cfg.C, out=s["pack_dst"])
+    elif name == "attn_split":
+        vf.attn_split(s["split_src"], cfg.P, cfg.C, out=s["split_dst"])
+    elif name == "head_merge":
+        vf.head_merge(s["merge_src"], cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, out=s["merge_dst"])
+    else:
+        vf.qkv_unpack(s["recv"], cfg.T, cfg.H, cfg.D, cfg.P, cfg.C, outs=s["qkv_out"])
+
+
+def back_to_back(vf, cfg, sets, ops_run, launches: int = 100, reps: int = 3):
+    """Per op: `launches` launches of that op alone, back to back on the
+    rotating buffer sets, with events only before the first and after the
+    last, so consecutive launches overlap as they do in the timed step; the
+    median over `reps` of total / launches, in microseconds."""
+    import torch
+    out = {}
+    for name in ops_run:
+        ts = []
+        for rep in range(reps + 1):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(launches):
+                run_op(vf, cfg, sets[i % len(sets)], name)
+            b.record()
+            if rep:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        out[name] = statistics.median(x.elapsed_time(y) for x, y in ts) * 1e3 / launches
+    return out
+
+
 def run_step(vf, cfg, s, events=None):
     """Enqueue the step's relayouts; events[i] is recorded before op i and
     events[-1] after the last one."""
@@ -455,11 +654,6 @@ def gpu_arm(args, rank, world, local_rank):
     barrier()
 
     K = args.steps
-    # per-op events on every `event_every`-th step only: an event between two
-    # kernels stops the next launch from overlapping the previous one's tail
-    every = max(1, args.event_every)
-    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(len(ops_run) + 1)]
-          for i in range(0, K, every)}
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
@@ -468,16 +662,27 @@ def gpu_arm(args, rank, world, local_rank):
     barrier()
     start.record()
     for i in range(K):
-        run_step(vf, cfg, sets[i % len(sets)], ev.get(i))
+        run_step(vf, cfg, sets[i % len(sets)])
     end.record()
     barrier()
+    # Per-op durations: an instrumented pass right after the timed region, with
+    # events around every op of every step (events between two kernels stop
+    # the next launch from overlapping the previous one's tail, so the timed
+    # region itself carries none).  Its first step is dropped; medians.
+    n_ev = max(50, args.event_steps) + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops_run) + 1)]
+          for _ in range(n_ev)]
+    for i in range(n_ev):
+        run_step(vf, cfg, sets[i % len(sets)], ev[i])
+    torch.cuda.synchronize()
     clock_info = clocks.stop()
 
+    b2b = back_to_back(vf, cfg, sets, ops_run)
+
     total_ms = start.elapsed_time(end)
-    per_op_ms = {name: [] for name in ops_run}
-    for e in ev.values():
-        for j, name in enumerate(ops_run):
-            per_op_ms[name].append(e[j].elapsed_time(e[j + 1]))
+    per_op_ms = {name: [e[j].elapsed_time(e[j + 1]) for e in ev[1:]]
+                 for j, name in enumerate(ops_run)}
+    inst_step_ms = [e[0].elapsed_time(e[-1]) for e in ev[1:]]
 
     max_ms = max_over_ranks(total_ms, dev)
 
@@ -486,29 +691,63 @@ def gpu_arm(args, rank, world, local_rank):
     value = job_gbs(step_bytes, K, world, max_ms)
     peak, peak_kind = measured_peak()
 
+    step_us = max_ms / K * 1e3
     ops = {}
     for name, ts in per_op_ms.items():
         med = statistics.median(ts)
-        mean = statistics.fmean(ts)
         b = alg_bytes(elems[name])
+        gbs = b / (med / 1e3) / 1e9
         ops[name] = {"bytes": b, "median_us": round(med * 1e3, 2),
-                     "mean_us": round(mean * 1e3, 2),
+                     "mean_us": round(statistics.fmean(ts) * 1e3, 2),
                      "min_us": round(min(ts) * 1e3, 2),
                      "p90_us": round(sorted(ts)[int(0.9 * (len(ts) - 1))] * 1e3, 2),
-                     "gbs": round(b / (med / 1e3) / 1e9, 1),
-                     "frac_of_peak": round(b / (med / 1e3) / 1e9 / peak, 4)}
+                     "samples": len(ts),
+                     "gbs": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4),
+                     "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                     "share_of_step": round(med * 1e3 / step_us, 4),
+                     "back_to_back_us": round(b2b[name], 2),
+                     "back_to_back_gbs": round(b / (b2b[name] / 1e6) / 1e9, 1)}
     if "attn_split" in ops:
         ops["attn_split"]["per_chunk_call_us"] = split_per_chunk_calls(vf, cfg, sets[0])
+    inst_med = statistics.median(inst_step_ms) * 1e3
+    per_op_summary = {
+        "method": "events around every op of %d instrumented steps run right after the "
+                  "timed region (first dropped); medians" % (n_ev - 1),
+        "instrumented_step_us": round(inst_med, 2),
+        "sum_of_op_medians_us": round(sum(o["median_us"] for o in ops.values()), 2),
+        "back_to_back": "per op, 100 launches of that op alone on the rotating sets, events "
+                        "only at the ends (launches overlap as in the timed step); median "
+                        "of 3 of total / 100",
+        "sum_of_back_to_back_us": round(sum(b2b.values()), 2),
+        "timed_step_us": round(step_us, 2),
+        "note": "the timed region has no events between ops, so consecutive launches "
+                "overlap (programmatic dependent launch) and its step is shorter than "
+                "an instrumented one; the back-to-back figures keep that overlap"}
 
-    dominant = max(per_op_ms, key=lambda k: sum(per_op_ms[k]))
-    avg_s = statistics.fmean(per_op_ms[dominant]) / 1e3
-    achieved = alg_bytes(elems[dominant]) / avg_s / 1e9
+    dominant = max(ops_run, key=lambda k: statistics.median(per_op_ms[k]))
+    dom_s = statistics.median(per_op_ms[dominant]) / 1e3
+    achieved = alg_bytes(elems[dominant]) / dom_s / 1e9
     traffic = recorded_traffic()
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
+                "nominal_peak": NOMINAL_HBM_GBS,
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": (traffic or {}).get(dominant),
-                "algorithmic_bytes": alg_bytes(elems[dominant])}
+                "algorithmic_bytes": alg_bytes(elems[dominant]),
+                "duration_us": round(dom_s * 1e6, 2),
+                "duration_stat": per_op_summary["method"],
+                "share_of_step": round(dom_s * 1e6 / step_us, 4)}
+    target = None
+    if cfg.name == "pages":
+        worst = min(ops[o]["frac_of_nominal"] for o in ("qkv_pack", "attn_split", "head_merge")
+                    if o in ops)
+        target = {"rule": "each relayout sustains >= 0.80 of GB300 HBM peak at the pages' "
+                          "shape",
+                  "judged_against": "the nominal %d GB/s (the stricter of the two; the "
+                                    "measured copy peak is %.1f GB/s)" % (NOMINAL_HBM_GBS, peak),
+                  "worst_op_frac_of_nominal": worst, "met": worst >= 0.80}
 
     e2e = None
     if not args.no_e2e and not args.only:
@@ -543,9 +782,12 @@ def gpu_arm(args, rank, world, local_rank):
                        "step": " + ".join(ops_run),
                        "l2": "inputs larger than L2 (each op reads >= 397 MB), "
                              "%d rotating buffer set(s)" % args.sets,
-                       "per_op_events": "every %d-th timed step" % every,
+                       "per_op_events": "%d instrumented steps after the timed region"
+                                        % (n_ev - 1),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "ops": ops,
+            "per_op_timing": per_op_summary,
+            "target": target,
             "roofline": roofline,
             "clocks": clock_info,
             "gpu_launches": K * launches_per_step(cfg, ops_run),
@@ -947,7 +1189,8 @@ def per_config(args, dev):
             med = statistics.median(x.elapsed_time(y) for x, y in ts)
             gbs = nbytes / (med / 1e3) / 1e9
             row[op] = {"us": round(med * 1e3, 2), "gbs": round(gbs, 1),
-                       "frac_of_peak": round(gbs / peak, 4)}
+                       "frac_of_peak": round(gbs / peak, 4),
+                       "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
         table[name] = row
         del pack_src, split_src, merge_src, merge_dst, recv, outs, pack_dst, split_dst
         del q_pack, q_pack_s, q_split, q_split_s, q_recv, q_recv_s, merge_bf16, outs_bf16
@@ -984,8 +1227,9 @@ def reference_arm(args, world):
         "ms_per_step": round(total / max(1, len(timed)) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded uniform 16-bit patterns)",
-        "config": {"workload": "%s: T=%d H=%d D=%d P=%d C=%d" % (cfg.name, cfg.T, cfg.H, cfg.D,
-                                                                cfg.P, cfg.C),
+        "config": {"workload": "%s (sampled: %d of %d tokens per core per step): T=%d H=%d "
+                               "D=%d P=%d C=%d" % (cfg.name, tokens, cfg.T, cfg.T, cfg.H, cfg.D,
+                                                   cfg.P, cfg.C),
                    "step": "qkv_pack + attn_split + head_merge (CPU oracle)",
                    "parallelism": "%d host processes" % cores},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
@@ -1014,8 +1258,9 @@ def main():
     ap.add_argument("--configs", nargs="*", default=["tiny", "4k", "pages", "ragged", "large"],
                     help="workloads for the per-op, per-workload table (none to skip)")
     ap.add_argument("--config-reps", type=int, default=30)
-    ap.add_argument("--event-every", type=int, default=10,
-                    help="record per-op events on every N-th timed step")
+    ap.add_argument("--event-steps", type=int, default=200,
+                    help="instrumented steps (at least 50) run after the timed region for "
+                         "the per-op durations")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the A/B/A comparison with the PyTorch materialisation chains")
     args = ap.parse_args()
@@ -1048,6 +1293,13 @@ def main():
                                                 cores=args.cpu_cores or None)
             line["cpu_baseline"]["lossy_single_core"] = lossy_cpu_baseline(
                 W.CONFIGS[args.config])
+            if line.get("per_config"):
+                cpu = cpu_per_config(list(line["per_config"]["table"]),
+                                     cores=args.cpu_cores or None)
+                for name, row in cpu.pop("table").items():
+                    for op, v in row.items():
+                        line["per_config"]["table"][name][op].update(v)
+                line["per_config"]["cpu"] = cpu
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)
