@@ -105,9 +105,6 @@ static_assert(kQuantThreads % 32 == 0 && kDequantThreads % 32 == 0,
 #ifndef VF_QUANT_F32X2
 #define VF_QUANT_F32X2 1
 #endif
-#ifndef VF_QUANT_DIV_TABLE
-#define VF_QUANT_DIV_TABLE 1
-#endif
 constexpr int kMantissas = 128;            // bfloat16 stored-mantissa patterns
 
 // Head rows in flight per group on the 8-element quantising path with NV
@@ -496,18 +493,16 @@ template <int FMT, int NV>
 __global__ void __launch_bounds__(kQuantThreads)
 quantise_rows8(const __grid_constant__ QArgs a) {
     constexpr int kRows = quant_rows8(NV);
-    const float top = top_code<FMT>();
-#if VF_QUANT_DIV_TABLE
-    // fl(top / M) and fl(M / top) for the 128 mantissas M = 1 + j/128, built
+    // fl(top / M) and fl(M / top) for the 128 mantissas M = 1 + i/128, built
     // before the grid-dependency wait (it overlaps the previous grid's tail)
+    const float top = top_code<FMT>();
     __shared__ float inv_of[kMantissas], scale_of[kMantissas];
-    for (int j = int(threadIdx.x); j < kMantissas; j += kQuantThreads) {
-        const float M = 1.0f + float(j) * (1.0f / 128.0f);      // exact
-        inv_of[j] = __fdiv_rn(top, M);
-        scale_of[j] = __fdiv_rn(M, top);
+    for (int i = int(threadIdx.x); i < kMantissas; i += kQuantThreads) {
+        const float M = 1.0f + float(i) * (1.0f / 128.0f);      // exact
+        inv_of[i] = __fdiv_rn(top, M);
+        scale_of[i] = __fdiv_rn(M, top);
     }
     __syncthreads();
-#endif
     wait_for_previous_grid();
     const QPiece &pc = a.pieces[blockIdx.y];
     const uint32_t G = 1u << a.lanes_log2;
@@ -550,17 +545,12 @@ quantise_rows8(const __grid_constant__ QArgs a) {
             // m[r]: the row's largest magnitude as a bfloat16 pattern
             const bool lost = non_finite_magnitude(m[r]);
             const bool live = !lost && m[r] >= 0x0F80u;           // amax >= 2^-96 (31 << 7)
-#if VF_QUANT_DIV_TABLE
-            // amax = M * 2^k: mantissa index j, exponent k = e - 127
-            const uint32_t j = m[r] & 0x7Fu;
+            // amax = M * 2^k: mantissa index mi, exponent k = e - 127 (both
+            // used only for a live row, whose results stay normal)
+            const uint32_t mi = m[r] & 0x7Fu;
             const uint32_t k23 = uint32_t((int32_t(m[r] >> 7) - 127) * (1 << 23));  // k << 23
-            const float inv = live ? __uint_as_float(__float_as_uint(inv_of[j]) - k23) : 0.0f;
-            const float scale = __uint_as_float(__float_as_uint(scale_of[j]) + k23);
-#else
-            const float amax = bf16_bits_to_float(m[r]);
-            const float inv = live ? __fdiv_rn(top, amax) : 0.0f;
-            const float scale = live ? __fdiv_rn(amax, top) : 0.0f;
-#endif
+            const float inv = live ? __uint_as_float(__float_as_uint(inv_of[mi]) - k23) : 0.0f;
+            const float scale = __uint_as_float(__float_as_uint(scale_of[mi]) + k23);
             const int64_t prow = pc.first_row + hr;               // packed head row
             uint8_t *crow = a.codes + prow * a.D;
             if (lane == 0)
