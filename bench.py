@@ -780,6 +780,7 @@ def gpu_arm(args, rank, world, local_rank):
                        "split_source": "head-major [H,T,D] viewed as [T,H,D]",
                        "merge_destination": "contiguous [T,H,D]",
                        "step": " + ".join(ops_run),
+                       "kernel_source_sha": kernel_source_hash(),
                        "l2": "inputs larger than L2 (each op reads >= 397 MB), "
                              "%d rotating buffer set(s)" % args.sets,
                        "per_op_events": "%d instrumented steps after the timed region"

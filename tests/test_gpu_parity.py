@@ -295,6 +295,56 @@ def test_non_default_stream_and_no_allocation():
     assert same_bits(out, loops.qkv_pack(src.cpu(), cfg.P, cfg.C))
 
 
+def test_every_op_allocates_nothing():
+    """The library allocates no device memory: after one warm-up call per op
+    (the first launch of a kernel loads its code), further calls of every
+    exact and lossy entry point change neither PyTorch's allocator count nor
+    the device's free memory as the driver reports it (which would also see a
+    cudaMalloc inside the library)."""
+    cfg = W.CONFIGS["4k"]
+    T, H, D, P, C = cfg.T, cfg.H, cfg.D, cfg.P, cfg.C
+    Hp = H // P
+    src, _ = W.pack_source(cfg, device=DEV)
+    s3, _ = W.split_source(cfg, device=DEV)
+    W.finite_rows_(src, 3)
+    W.finite_rows_(s3, 4)
+    m = W.merge_source(cfg, device=DEV)
+    recv = W.fill_(torch.empty(3 * T * Hp * D, dtype=torch.int16, device=DEV), "normal", 9)
+    pk = torch.empty(3 * T * H * D, dtype=torch.int16, device=DEV)
+    sp = torch.empty(T * H * D, dtype=torch.int16, device=DEV)
+    mg = torch.empty((T, H, D), dtype=torch.int16, device=DEV)
+    qkv = tuple(torch.empty((T, Hp, D), dtype=torch.int16, device=DEV) for _ in range(3))
+    qc = torch.empty(3 * T * H * D, dtype=torch.int8, device=DEV)
+    qs = torch.empty(3 * T * H, dtype=torch.float32, device=DEV)
+    fc = torch.empty(T * H * D, dtype=torch.float8_e4m3fn, device=DEV)
+    fs = torch.empty(T * H, dtype=torch.float32, device=DEV)
+    bq = tuple(t.view(torch.bfloat16) for t in qkv)
+    calls = [
+        lambda: vf.qkv_pack(src, P, C, out=pk),
+        lambda: vf.qkv_pack(src, P, C, out=pk, order="slot_major", chunks=(1, 2)),
+        lambda: vf.qkv_pack3(src[:, 0], src[:, 1], src[:, 2], P, C, out=pk),
+        lambda: vf.attn_split(s3, P, C, out=sp),
+        lambda: vf.head_merge(m, T, H, D, P, C, out=mg),
+        lambda: vf.qkv_unpack(recv, T, H, D, P, C, outs=qkv),
+        lambda: vf.qkv_pack_q(src, P, C, fmt="int8", codes=qc, scales=qs),
+        lambda: vf.qkv_unpack_q(qc[:3 * T * Hp * D], qs[:3 * T * Hp], T, H, D, P, C,
+                                fmt="int8", outs=bq),
+        lambda: vf.attn_split_q(s3, P, C, fmt="e4m3", codes=fc, scales=fs),
+        lambda: vf.head_merge_q(fc, fs, T, H, D, P, C, fmt="e4m3", out=mg.view(torch.bfloat16)),
+    ]
+    for fn in calls:                       # warm-up: code modules load on first use
+        fn()
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_allocated(DEV)
+    free_before, _ = torch.cuda.mem_get_info(DEV)
+    for _ in range(3):
+        for fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(DEV) == before
+    assert torch.cuda.mem_get_info(DEV)[0] == free_before
+
+
 def test_rejections_do_not_touch_destination():
     x4 = rand_bits((8, 3, 4, 8), 1)
     out = torch.zeros(3 * 8 * 4 * 8, dtype=torch.int16, device=DEV)
