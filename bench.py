@@ -649,16 +649,16 @@ def gpu_arm(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for i in range(args.warmup):
-        run_step(vf, cfg, sets[i % len(sets)])
-    barrier()
-
     K = args.steps
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    # the clock sampler needs a moment to start; the warm-up steps come after
+    # that pause, right before the timed region, so that it starts warm
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
+    for i in range(args.warmup):
+        run_step(vf, cfg, sets[i % len(sets)])
     barrier()
     start.record()
     for i in range(K):
