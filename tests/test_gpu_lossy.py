@@ -320,21 +320,23 @@ def test_pages_workload_in_full():
     codes, scales = vf.qkv_pack_q(x, P, C, fmt="int8")
     wc, ws = loops.qkv_pack_q(x.cpu(), P, C, loops.INT8)
     assert torch.equal(u8(codes), u8(wc)) and torch.equal(i32(scales), i32(ws))
-    del x
+    del x, codes, scales
+    # the receive side takes the oracle's own codes and scales (one rank's worth)
     Hp = H // P
-    rc, rs = codes[:3 * T * Hp * D], scales[:3 * T * Hp]      # one rank's worth, valid codes
-    outs = vf.qkv_unpack_q(rc, rs, T, H, D, P, C, fmt="int8")
-    want = loops.qkv_unpack_q(u8(rc), rs.cpu(), T, H, D, P, C, loops.INT8)
+    rc, rs = wc[:3 * T * Hp * D].contiguous(), ws[:3 * T * Hp].contiguous()
+    outs = vf.qkv_unpack_q(rc.to(DEV), rs.to(DEV), T, H, D, P, C, fmt="int8")
+    want = loops.qkv_unpack_q(rc, rs, T, H, D, P, C, loops.INT8)
     for o, w in zip(outs, want):
         assert torch.equal(o.view(torch.int16).cpu(), w)
-    del outs, want, codes, scales, wc, ws
+    del outs, want, wc, ws, rc, rs
 
     a = split_view(T, H, D, "bhtd", seed=72)
     fc, fs = vf.attn_split_q(a, P, C, fmt="e4m3")
     wc, ws = loops.attn_split_q(a.cpu(), P, C, loops.E4M3)
     assert torch.equal(u8(fc), u8(wc)) and torch.equal(i32(fs), i32(ws))
-    out = vf.head_merge_q(fc, fs, T, H, D, P, C, fmt="e4m3")
-    want = loops.head_merge_q(u8(fc), fs.cpu(), T, H, D, P, C, loops.E4M3)
+    del fc, fs
+    out = vf.head_merge_q(wc.to(DEV), ws.to(DEV), T, H, D, P, C, fmt="e4m3")
+    want = loops.head_merge_q(wc, ws, T, H, D, P, C, loops.E4M3)
     assert torch.equal(out.view(torch.int16).cpu(), want)
 
 

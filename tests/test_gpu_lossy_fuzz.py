@@ -98,22 +98,25 @@ def test_lossy_fuzz(seed):
     n = T * H * D
     codes, scales = codes_buffer(n, fmt, coff), torch.empty(n // D, device=DEV)
     vf.attn_split_q(x3, P, C, fmt=fmt, codes=codes, scales=scales, order=order)
-    wc, ws = loops.attn_split_q(x3.cpu(), P, C, f)
-    wc = wc.view(torch.uint8)
+    mc, ms = loops.attn_split_q(x3.cpu(), P, C, f)             # the oracle's, chunk-major
+    mc = mc.view(torch.uint8)
+    wc, ws = mc, ms
     if order == "slot_major":
         wc = slot_major(1, wc, T, H, D, P, C, 1)
         ws = slot_major(1, ws, T, H, D, P, C, D)
     assert torch.equal(codes.view(torch.uint8).cpu(), wc), (seed, "split codes")
     assert torch.equal(scales.cpu().view(torch.int32), ws.view(torch.int32)), (seed, "split scales")
 
-    # dequantising merge: the split's storage of a full-head view at P
+    # dequantising merge of the oracle's split storage (a full-head view at P),
+    # given to the kernel in the block order under test, at a code offset
     out = strided_view((T, H, D), layout if layout != "dstride2" else "contiguous", offset)
-    vf.head_merge_q(codes, scales, T, H, D, P, C, fmt=fmt, out=out.view(torch.bfloat16),
+    rc = codes_buffer(n, fmt, coff)
+    rc.view(torch.uint8).copy_(wc)
+    vf.head_merge_q(rc, ws.to(DEV), T, H, D, P, C, fmt=fmt, out=out.view(torch.bfloat16),
                     order=order)
-    mc, ms = codes.view(torch.uint8).cpu(), scales.cpu()
-    if order == "slot_major":
-        mc = chunk_major(2, mc, T, H, D, P, C, 1)
-        ms = chunk_major(2, ms, T, H, D, P, C, D)
+    if order == "slot_major":          # the same bytes read as the merge's (c, p) blocks
+        mc = chunk_major(2, wc, T, H, D, P, C, 1)
+        ms = chunk_major(2, ws, T, H, D, P, C, D)
     want = loops.head_merge_q(mc, ms, T, H, D, P, C, f)
     assert torch.equal(out.cpu(), want), (seed, "merge")
 
