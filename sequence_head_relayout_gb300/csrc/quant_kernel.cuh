@@ -84,7 +84,7 @@ namespace vf {
 #define VF_QUANT_ROWS 2
 #endif
 #ifndef VF_QUANT_ROWS_SHORT
-#define VF_QUANT_ROWS_SHORT 3
+#define VF_QUANT_ROWS_SHORT 4
 #endif
 #ifndef VF_DEQUANT_ROWS
 #define VF_DEQUANT_ROWS 1
