@@ -147,6 +147,32 @@ int main(void) {
             } else {
                 CHECK(cudaMemcpy(h_y, d_packed, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
                 CHECK(memcmp(h_y, h_x, n * 2) == 0);
+                /* a head row holding a NaN and one holding an infinity are lost rows:
+                 * each gets the float32 quiet NaN as its scale, and every element of
+                 * theirs arrives as the bfloat16 quiet NaN; no other row changes */
+                const int64_t rows = n / D, r1 = 5, r2 = rows - 3;   /* [T][3H][D] rows */
+                h_x[r1 * D + 7] = 0x7FC1;
+                h_x[r2 * D] = 0xFF80;
+                CHECK(cudaMemcpy(d_src, h_x, n * 2, cudaMemcpyHostToDevice) == cudaSuccess);
+                const int64_t s3[3] = {3 * H * D, D, 1};
+                CHECK(vf_attn_split_fp8(d_src, s3, T, 3 * H, D, P, C, d_codes, d_scales,
+                                        NULL) == VF_OK);
+                CHECK(vf_head_merge_fp8(d_codes, d_scales, NULL, T, 3 * H, D, P, C, d_packed,
+                                        NULL) == VF_OK);
+                CHECK(cudaDeviceSynchronize() == cudaSuccess);
+                CHECK(cudaMemcpy(h_s, d_scales, rows * sizeof(float), cudaMemcpyDeviceToHost) ==
+                      cudaSuccess);
+                int lost = 0;
+                for (int64_t r = 0; r < rows; ++r) {
+                    uint32_t b;
+                    memcpy(&b, &h_s[r], 4);
+                    lost += b == 0x7FC00000u;
+                }
+                CHECK(lost == 2);
+                CHECK(cudaMemcpy(h_y, d_packed, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
+                for (int64_t r = 0; r < rows; ++r)
+                    for (int64_t d = 0; d < D; ++d)
+                        CHECK(h_y[r * D + d] == ((r == r1 || r == r2) ? 0x7FC0 : h_x[r * D + d]));
             }
             cudaFree(d_codes);
             cudaFree(d_scales);
